@@ -1,0 +1,343 @@
+/*
+ * oracle.c -- plain CPU oracle for the clipped-AdamW optimizer step and the
+ * step_NNNNNN.bin checkpoint.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no source, header, constant or helper with the
+ * CUDA library: it restates the method from the pages it was written from,
+ * one definition at a time, in double precision over float32 state, with no
+ * blocking, fusion or reordering beyond what those definitions state.
+ *
+ * Sources (cited by page title and section):
+ *  [T]  "Training as a Recoverable State Transition" (aihero.club, Language
+ *       Models from Scratch): sections "The Exact Targets of Clipping and
+ *       AdamW", "Example 1: The First One-Dimensional Step and Moment State",
+ *       and "The Checkpoint Contract and a Real Recovery Test".
+ *  [C]  "Grow a Language Model: Checkpoints" (unhomeschool.com, Georgian and
+ *       Spanish editions): sections "Format", "Region by region",
+ *       "Total size", "Why save m & v".
+ *  [S]  "Checkpoint and Sharded Resume" (AI Engineering from Scratch, phase 19
+ *       lesson 80): sections "Atomic write" and "Three failure modes".
+ *
+ * Build: any C99 compiler, -O2 -ffp-contract=off (no fused multiply-add, so
+ * that every operation below is one IEEE double rounding on x86 and Arm
+ * alike), no -ffast-math.
+ */
+#define _POSIX_C_SOURCE 200809L
+#include <errno.h>
+#include <fcntl.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+#include <sys/stat.h>
+#include <unistd.h>
+
+/* Status codes of this file (its own; the CUDA library has its own set). */
+#define OR_OK 0
+#define OR_EINVAL 1     /* bad argument                                    */
+#define OR_EIO 2        /* open/read/write/fsync/rename failed             */
+#define OR_EFORMAT 3    /* header fields impossible (negative step or n)   */
+#define OR_ESIZE 4      /* file size disagrees with 8 + 12 n, or truncated */
+#define OR_EMISMATCH 5  /* n in the file differs from the expected n       */
+#define OR_ENONFINITE 6 /* gradient norm is inf or nan: state left as is   */
+
+int oracle_version(void) { return 1; }
+
+/* ------------------------------------------------------------------------
+ * Global L2 norm of the concatenated gradient.  [T] "The Exact Targets of
+ * Clipping and AdamW": all parameter gradients are joined into one vector g
+ * and its Euclidean norm ||g||_2 is taken.  Each float32 value is widened to
+ * double; its square is exact in double (24-bit significand squared fits in
+ * 53 bits); the squares are summed in index order.
+ * ---------------------------------------------------------------------- */
+double oracle_sumsq(const float* g, int64_t n)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double x = (double)g[i];
+        s = s + x * x;
+    }
+    return s;
+}
+
+double oracle_global_norm(const float* g, int64_t n)
+{
+    return sqrt(oracle_sumsq(g, n));
+}
+
+/* ------------------------------------------------------------------------
+ * Clip factor.  [T] "The Exact Targets of Clipping and AdamW": when the norm
+ * exceeds the threshold c the whole vector is multiplied by c/||g||,
+ * otherwise it is left unchanged; one c for all layers.  The worked code on
+ * that page uses min(1, c/|g|), i.e. a strict ">" and no epsilon; a zero
+ * norm therefore never divides.
+ * ---------------------------------------------------------------------- */
+double oracle_clip_scale(double norm, double c)
+{
+    if (norm > c)
+        return c / norm;
+    return 1.0;
+}
+
+/* ------------------------------------------------------------------------
+ * One AdamW update of one parameter, every intermediate in double.
+ * [T] "The Exact Targets of Clipping and AdamW":
+ *   m_t = beta1 m + (1-beta1) g          (first moment, EMA of gradients)
+ *   v_t = beta2 v + (1-beta2) g^2        (second moment, EMA of squares)
+ *   m_hat = m_t / (1 - beta1^t)          (bias correction, t counts updates
+ *   v_hat = v_t / (1 - beta2^t)           and the first update has t = 1)
+ *   w <- w (1 - lr wd) - lr m_hat / (sqrt(v_hat) + eps)
+ * The decay multiplies the old weight first and is applied to every
+ * parameter; eps is added to sqrt(v_hat), not to v.  Here g is the already
+ * clipped gradient g_hat = s * g.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double g_hat;     /* clipped gradient s*g                    */
+    double m;         /* new first moment m_t                    */
+    double v;         /* new second moment v_t                   */
+    double m_hat;     /* bias-corrected first moment             */
+    double v_hat;     /* bias-corrected second moment            */
+    double w_decayed; /* w (1 - lr wd)                           */
+    double update;    /* lr m_hat / (sqrt(v_hat) + eps)          */
+    double w;         /* new weight w_decayed - update           */
+} oracle_terms;
+
+void oracle_adamw_element(double w, double g, double m, double v, double s,
+                          int32_t t, double lr, double wd, double beta1,
+                          double beta2, double eps, oracle_terms* out)
+{
+    double g_hat = g * s;
+    double m_t = beta1 * m + (1.0 - beta1) * g_hat;
+    double v_t = beta2 * v + (1.0 - beta2) * (g_hat * g_hat);
+    double m_hat = m_t / (1.0 - pow(beta1, (double)t));
+    double v_hat = v_t / (1.0 - pow(beta2, (double)t));
+    double w_decayed = w * (1.0 - lr * wd);
+    double update = lr * m_hat / (sqrt(v_hat) + eps);
+    out->g_hat = g_hat;
+    out->m = m_t;
+    out->v = v_t;
+    out->m_hat = m_hat;
+    out->v_hat = v_hat;
+    out->w_decayed = w_decayed;
+    out->update = update;
+    out->w = w_decayed - update;
+}
+
+/* ------------------------------------------------------------------------
+ * One full optimizer step over the flat float32 state: global norm, clip
+ * factor, AdamW per element, each new value rounded to float32 once.
+ * [T] "The Exact Targets of Clipping and AdamW" (the step order: record the
+ * norm, clip globally, then step).  A non-finite norm leaves w, m, v as they
+ * are and returns OR_ENONFINITE (the page asks only that norms be recorded
+ * to detect numerical faults; skipping the update is this oracle's reading).
+ * ---------------------------------------------------------------------- */
+int oracle_adamw_clip_step(float* w, const float* g, float* m, float* v,
+                           int64_t n, int32_t t, double lr, double wd,
+                           double clip, double beta1, double beta2, double eps,
+                           double* norm_out)
+{
+    if (n < 0 || t < 1)
+        return OR_EINVAL;
+    double norm = oracle_global_norm(g, n);
+    if (norm_out)
+        *norm_out = norm;
+    if (!isfinite(norm))
+        return OR_ENONFINITE;
+    double s = oracle_clip_scale(norm, clip);
+    for (int64_t i = 0; i < n; ++i) {
+        oracle_terms r;
+        oracle_adamw_element((double)w[i], (double)g[i], (double)m[i],
+                             (double)v[i], s, t, lr, wd, beta1, beta2, eps, &r);
+        w[i] = (float)r.w;
+        m[i] = (float)r.m;
+        v[i] = (float)r.v;
+    }
+    return OR_OK;
+}
+
+/* The same update at chosen indices only, given the clip factor s (from a
+ * full-vector norm computed separately).  Used to check outputs of a large
+ * state one element at a time.  Results go to the *_out arrays. */
+void oracle_adamw_at(const int64_t* idx, int64_t k, const float* w,
+                     const float* g, const float* m, const float* v, double s,
+                     int32_t t, double lr, double wd, double beta1,
+                     double beta2, double eps, float* w_out, float* m_out,
+                     float* v_out)
+{
+    for (int64_t j = 0; j < k; ++j) {
+        int64_t i = idx[j];
+        oracle_terms r;
+        oracle_adamw_element((double)w[i], (double)g[i], (double)m[i],
+                             (double)v[i], s, t, lr, wd, beta1, beta2, eps, &r);
+        w_out[j] = (float)r.w;
+        m_out[j] = (float)r.m;
+        v_out[j] = (float)r.v;
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * The step_NNNNNN.bin image.  [C] "Format" / "Region by region" /
+ * "Total size": five contiguous regions
+ *     [int32 step][int32 n_params][n x f32 weights][n x f32 m][n x f32 v],
+ * 8 + 12 n bytes in total, no other metadata.  The pages do not state the
+ * byte order; this oracle writes little-endian two's-complement integers and
+ * little-endian IEEE binary32 floats, one byte at a time for the header so
+ * that the order is explicit.
+ * ---------------------------------------------------------------------- */
+static void put_le32(unsigned char* p, uint32_t x)
+{
+    p[0] = (unsigned char)(x & 0xffu);
+    p[1] = (unsigned char)((x >> 8) & 0xffu);
+    p[2] = (unsigned char)((x >> 16) & 0xffu);
+    p[3] = (unsigned char)((x >> 24) & 0xffu);
+}
+
+static uint32_t get_le32(const unsigned char* p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) |
+           ((uint32_t)p[3] << 24);
+}
+
+static int host_is_little_endian(void)
+{
+    uint32_t one = 1;
+    unsigned char b;
+    memcpy(&b, &one, 1);
+    return b == 1;
+}
+
+int64_t oracle_ckpt_size(int64_t n) { return 8 + 12 * n; }
+
+/* Writes the 8 + 12 n byte image into out. */
+int oracle_pack(int32_t step, int32_t n, const float* w, const float* m,
+                const float* v, unsigned char* out)
+{
+    if (n < 0 || step < 0 || !host_is_little_endian())
+        return OR_EINVAL;
+    put_le32(out, (uint32_t)step);
+    put_le32(out + 4, (uint32_t)n);
+    size_t bytes = (size_t)n * 4u;
+    memcpy(out + 8, w, bytes);
+    memcpy(out + 8 + bytes, m, bytes);
+    memcpy(out + 8 + 2 * bytes, v, bytes);
+    return OR_OK;
+}
+
+static int write_all(FILE* f, const void* p, size_t bytes)
+{
+    return fwrite(p, 1, bytes, f) == bytes ? OR_OK : OR_EIO;
+}
+
+/* ------------------------------------------------------------------------
+ * Atomic checkpoint write.  [S] "Atomic write": write the data to
+ * <name>.tmp, fsync it, then rename over the final name; POSIX rename on one
+ * file system is atomic, so a crash before the rename leaves the previous
+ * checkpoint live.  The directory is fsynced after the rename so that the
+ * new name itself is durable.  File name: step_%06d.bin ([C] uses
+ * step_NNNNNN.bin and step_112700.bin).
+ * ---------------------------------------------------------------------- */
+int oracle_ckpt_write(const char* dir, int32_t step, int32_t n, const float* w,
+                      const float* m, const float* v, char* path_out,
+                      size_t path_cap)
+{
+    if (!dir || n < 0 || step < 0 || !host_is_little_endian())
+        return OR_EINVAL;
+    char final_path[4096], tmp_path[4112];
+    int len = snprintf(final_path, sizeof final_path, "%s/step_%06d.bin", dir,
+                       (int)step);
+    if (len < 0 || (size_t)len >= sizeof final_path)
+        return OR_EINVAL;
+    snprintf(tmp_path, sizeof tmp_path, "%s.tmp", final_path);
+
+    FILE* f = fopen(tmp_path, "wb");
+    if (!f)
+        return OR_EIO;
+    unsigned char header[8];
+    put_le32(header, (uint32_t)step);
+    put_le32(header + 4, (uint32_t)n);
+    size_t bytes = (size_t)n * 4u;
+    int rc = write_all(f, header, 8);
+    if (rc == OR_OK)
+        rc = write_all(f, w, bytes);
+    if (rc == OR_OK)
+        rc = write_all(f, m, bytes);
+    if (rc == OR_OK)
+        rc = write_all(f, v, bytes);
+    if (rc == OR_OK && fflush(f) != 0)
+        rc = OR_EIO;
+    if (rc == OR_OK && fsync(fileno(f)) != 0)
+        rc = OR_EIO;
+    if (fclose(f) != 0 && rc == OR_OK)
+        rc = OR_EIO;
+    if (rc != OR_OK) {
+        unlink(tmp_path);
+        return rc;
+    }
+    if (rename(tmp_path, final_path) != 0) {
+        unlink(tmp_path);
+        return OR_EIO;
+    }
+    int dfd = open(dir, O_RDONLY);
+    if (dfd >= 0) {
+        fsync(dfd);
+        close(dfd);
+    }
+    if (path_out && path_cap > 0)
+        snprintf(path_out, path_cap, "%s", final_path);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Validating read.  [S] "Three failure modes" asks that a bad checkpoint be
+ * refused loudly instead of loaded silently; for the single-file format of
+ * [C] the checks available are: the header is readable, step and n are not
+ * negative, n equals the caller's parameter count, and the file holds
+ * exactly 8 + 12 n bytes (a partial write is shorter).  Only after all
+ * checks pass are w, m, v filled.
+ * ---------------------------------------------------------------------- */
+int oracle_ckpt_read(const char* path, int32_t n_expected, int32_t* step_out,
+                     float* w, float* m, float* v)
+{
+    if (!path || n_expected < 0 || !host_is_little_endian())
+        return OR_EINVAL;
+    FILE* f = fopen(path, "rb");
+    if (!f)
+        return OR_EIO;
+    struct stat st;
+    if (fstat(fileno(f), &st) != 0) {
+        fclose(f);
+        return OR_EIO;
+    }
+    unsigned char header[8];
+    if (st.st_size < 8 || fread(header, 1, 8, f) != 8) {
+        fclose(f);
+        return OR_ESIZE;
+    }
+    int32_t step = (int32_t)get_le32(header);
+    int32_t n = (int32_t)get_le32(header + 4);
+    if (step < 0 || n < 0) {
+        fclose(f);
+        return OR_EFORMAT;
+    }
+    if (n != n_expected) {
+        fclose(f);
+        return OR_EMISMATCH;
+    }
+    if ((int64_t)st.st_size != oracle_ckpt_size(n)) {
+        fclose(f);
+        return OR_ESIZE;
+    }
+    size_t bytes = (size_t)n * 4u;
+    if (fread(w, 1, bytes, f) != bytes || fread(m, 1, bytes, f) != bytes ||
+        fread(v, 1, bytes, f) != bytes) {
+        fclose(f);
+        return OR_ESIZE;
+    }
+    fclose(f);
+    if (step_out)
+        *step_out = step;
+    return OR_OK;
+}

@@ -1,0 +1,399 @@
+"""Pins of the CPU oracle: checks against what the pages and mathematics fix.
+
+Each pin takes an ``oracle.Oracle`` and a scratch directory and raises
+``AssertionError`` when the oracle disagrees with a printed value, a closed
+form, an invariant or an exact computation.  ``test_oracle_pins.py`` runs them
+on the oracle itself; ``test_oracle_mutants.py`` runs them on copies of the
+oracle with one planted mistake each and requires that some pin fails.
+
+None of the pins re-types the oracle's own formula: they use the pages'
+printed numbers (``golden/``), closed forms that follow from the definitions
+(t = 1, constant gradient, zero gradient), exact sums (``math.fsum``),
+Pythagorean triples, and the checkpoint's byte layout read back by hand.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import struct
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+B1, B2, EPS = 0.9, 0.999, 1e-8
+
+
+def read_golden(name):
+    inputs, expects, other = {}, {}, {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            if parts[0] == "input":
+                inputs[parts[1]] = float(parts[2])
+            elif parts[0] == "expect":
+                expects[parts[1]] = (float(parts[2]), float(parts[3]))
+            else:
+                other[parts[0]] = parts[1:]
+    return inputs, expects, other
+
+
+# --- the pages' worked example ---------------------------------------------
+
+def pin_example1(o, tmp):
+    """Example 1: m, v, bias-corrected moments, decayed and final weight."""
+    inp, exp, _ = read_golden("example1.txt")
+    s = o.clip_scale(abs(inp["g"]), inp["clip"])
+    r = o.adamw_element(inp["w"], inp["g"], 0.0, 0.0, s, int(inp["t"]),
+                        inp["lr"], inp["wd"])
+    r["scale"] = s
+    for k, (val, tol) in exp.items():
+        assert abs(r[k] - val) <= tol, (k, r[k], val, tol)
+
+
+def pin_example1_float32_state(o, tmp):
+    """Example 1 through the float32 vector step: same printed values after
+    one rounding to float32."""
+    inp, exp, _ = read_golden("example1.txt")
+    w = np.array([inp["w"]], np.float32)
+    g = np.array([inp["g"]], np.float32)
+    m = np.zeros(1, np.float32)
+    v = np.zeros(1, np.float32)
+    st, norm = o.adamw_clip_step(w, g, m, v, 1, inp["lr"], inp["wd"], inp["clip"])
+    assert st == 0 and norm == 0.5
+    for k, arr in (("w", w), ("m", m), ("v", v)):
+        val, tol = exp[k]
+        # one float32 rounding of the exact value, plus the printed tolerance
+        assert abs(float(arr[0]) - val) <= tol + abs(val) * 2.0 ** -24, (k, arr[0])
+
+
+def _scalar_step(o, state, g, clip, lr, wd):
+    w, m, v, t = state
+    s = o.clip_scale(abs(g), clip)
+    r = o.adamw_element(w, g, m, v, s, t + 1, lr, wd)
+    return [r["w"], r["m"], r["v"], t + 1]
+
+
+def pin_worked_code_resume(o, tmp):
+    """The worked code's three assertions (first step, exact resume from the
+    full state after a JSON round trip, weights-only resume diverges)."""
+    _, _, g = read_golden("worked_code_resume.txt")
+    w0 = float(g["w0"][0])
+    grads = [float(x) for x in g["grads"]]
+    clip, lr, wd = float(g["clip"][0]), float(g["lr"][0]), float(g["wd"][0])
+    state = [w0, 0.0, 0.0, 0]
+    first = _scalar_step(o, state, grads[0], clip, lr, wd)
+    assert abs(first[0] - float(g["first_w"][0])) < float(g["first_w"][1])
+    cont = state
+    for x in grads:
+        cont = _scalar_step(o, cont, x, clip, lr, wd)
+    prefix = state
+    for x in grads[:2]:
+        prefix = _scalar_step(o, prefix, x, clip, lr, wd)
+    resumed = _scalar_step(o, json.loads(json.dumps(prefix)), grads[2], clip, lr, wd)
+    assert cont == resumed
+    wrong = _scalar_step(o, [prefix[0], 0.0, 0.0, 0], grads[2], clip, lr, wd)
+    assert abs(wrong[0] - cont[0]) > float(g["weights_only_min_gap"][0])
+
+
+def pin_second_step_moments(o, tmp):
+    """Step 2 of the worked example (gradient -0.25): the moments are the
+    exponential averages 0.9*0.05 + 0.1*(-0.25) = 0.02 and
+    0.999*0.00025 + 0.001*0.0625 = 0.00031225 (hand arithmetic)."""
+    s1 = _scalar_step(o, [2.0, 0.0, 0.0, 0], 0.5, 1.0, 0.1, 0.01)
+    s2 = _scalar_step(o, s1, -0.25, 1.0, 0.1, 0.01)
+    assert abs(s2[1] - 0.02) < 1e-15 and abs(s2[2] - 0.00031225) < 1e-15
+    # bias-corrected: 0.02/(1-0.81) and 0.00031225/(1-0.998001)
+    r = o.adamw_element(s1[0], -0.25, s1[1], s1[2], 1.0, 2, 0.1, 0.01)
+    assert abs(r["m_hat"] - 0.02 / 0.19) < 1e-14
+    assert abs(r["v_hat"] - 0.00031225 / 0.001999) < 1e-13
+
+
+# --- AdamW closed forms ------------------------------------------------------
+
+def pin_t1_closed_form(o, tmp):
+    """At t = 1 from zero moments, m_hat = g_hat and v_hat = g_hat^2 for any
+    betas, so the update is lr*g_hat/(|g_hat| + eps)."""
+    rng = np.random.default_rng(1)
+    for b1, b2 in ((0.9, 0.999), (0.5, 0.7), (0.8, 0.95)):
+        for gh in list(rng.normal(0, 1, 8)) + [1e-8, -3e-9, 250.0]:
+            w, lr, wd = 0.75, 0.01, 0.1
+            r = o.adamw_element(w, gh, 0.0, 0.0, 1.0, 1, lr, wd, b1, b2, EPS)
+            want_upd = lr * gh / (abs(gh) + EPS)
+            assert math.isclose(r["m_hat"], gh, rel_tol=1e-14)
+            assert math.isclose(r["v_hat"], gh * gh, rel_tol=1e-14)
+            assert math.isclose(r["update"], want_upd, rel_tol=1e-13), (gh, r)
+            assert math.isclose(r["w"], w * (1 - lr * wd) - want_upd,
+                                rel_tol=1e-13, abs_tol=1e-15)
+
+
+def pin_eps_position(o, tmp):
+    """eps is added to sqrt(v_hat): a gradient equal to eps at t = 1 moves the
+    weight by exactly lr/2 (no decay)."""
+    r = o.adamw_element(1.0, EPS, 0.0, 0.0, 1.0, 1, 0.2, 0.0)
+    assert math.isclose(r["update"], 0.1, rel_tol=1e-12), r
+    assert math.isclose(r["w"], 0.9, rel_tol=1e-12)
+
+
+def pin_constant_gradient(o, tmp):
+    """A constant gradient gamma gives m_t = gamma (1-b1^t) and
+    v_t = gamma^2 (1-b2^t), so m_hat = gamma and v_hat = gamma^2 at every t:
+    each update is lr*gamma/(|gamma|+eps) and
+    w_t = w0 d^t - u (1 - d^t)/(1 - d) with d = 1 - lr wd."""
+    gamma, lr, wd, w0 = -0.3, 0.05, 0.2, 1.5
+    d = 1 - lr * wd
+    u = lr * gamma / (abs(gamma) + EPS)
+    state = [w0, 0.0, 0.0, 0]
+    for t in range(1, 41):
+        r = o.adamw_element(state[0], gamma, state[1], state[2], 1.0, t, lr, wd)
+        state = [r["w"], r["m"], r["v"], t]
+        assert math.isclose(r["m"], gamma * (1 - B1 ** t), rel_tol=1e-12)
+        assert math.isclose(r["v"], gamma * gamma * (1 - B2 ** t), rel_tol=1e-12)
+        assert math.isclose(r["m_hat"], gamma, rel_tol=1e-12), (t, r)
+        assert math.isclose(r["v_hat"], gamma * gamma, rel_tol=1e-12), (t, r)
+        want = w0 * d ** t - u * (1 - d ** t) / (1 - d)
+        assert math.isclose(r["w"], want, rel_tol=1e-12), (t, r["w"], want)
+
+
+def pin_zero_gradient(o, tmp):
+    """A zero gradient decays the weight only and shrinks the moments by the
+    betas: w' = w (1 - lr wd), m' = b1 m, v' = b2 v (with v > 0 the update
+    is lr m_hat/(sqrt(v_hat)+eps) of the shrunk moments)."""
+    r = o.adamw_element(3.0, 0.0, 0.0, 0.0, 1.0, 5, 0.01, 0.5)
+    assert r["update"] == 0.0 and math.isclose(r["w"], 3.0 * (1 - 0.005), rel_tol=1e-15)
+    r = o.adamw_element(3.0, 0.0, 0.2, 0.04, 1.0, 1, 0.01, 0.0)
+    assert math.isclose(r["m"], B1 * 0.2, rel_tol=1e-15)
+    assert math.isclose(r["v"], B2 * 0.04, rel_tol=1e-15)
+
+
+def pin_decay_on_every_parameter(o, tmp):
+    """Weight decay is decoupled and multiplies the OLD weight: with lr = 1e-3
+    and wd = 1, the decay term is w*lr*wd independent of the update."""
+    for w in (-2.0, 0.5, 4.0):
+        r = o.adamw_element(w, 0.25, 0.0, 0.0, 1.0, 1, 1e-3, 1.0)
+        assert math.isclose(r["w_decayed"], w * (1 - 1e-3), rel_tol=1e-15)
+        assert math.isclose(r["w"] - r["w_decayed"], -r["update"], rel_tol=1e-12)
+
+
+# --- norm and clip -----------------------------------------------------------
+
+def pin_norm_pythagorean(o, tmp):
+    for vec, want in (([3, 4], 5.0), ([1, 2, 2], 3.0), ([2, 3, 6], 7.0),
+                      ([-3, -4], 5.0), ([0, 0, 0], 0.0), ([8, 9, 12], 17.0)):
+        assert o.global_norm(np.array(vec, np.float32)) == want, vec
+
+
+def pin_norm_constant(o, tmp):
+    """g = k everywhere: ||g|| = |k| sqrt(n), exact for k = 0.5, n = 4096."""
+    assert o.global_norm(np.full(4096, 0.5, np.float32)) == 32.0
+    assert o.global_norm(np.full(10000, -0.25, np.float32)) == 25.0
+
+
+def pin_norm_exact_sum(o, tmp):
+    """Squares of float32 values are exact in double, so math.fsum of them is
+    the correctly rounded sum of squares; the index-order sum stays within
+    n ulps of it."""
+    rng = np.random.default_rng(2)
+    for n in (1, 7, 1000, 65537):
+        g = (rng.standard_normal(n) * rng.choice([1e-3, 1.0, 40.0], n)).astype(np.float32)
+        exact = math.fsum(float(x) * float(x) for x in g)
+        got = o.sumsq(g)
+        assert abs(got - exact) <= n * 2.3e-16 * exact, (n, got, exact)
+        assert math.isclose(o.global_norm(g), math.sqrt(exact), rel_tol=n * 2.3e-16)
+
+
+def pin_norm_homogeneous(o, tmp):
+    """||2^k g|| = 2^k ||g|| exactly (power-of-two scaling is exact)."""
+    g = np.random.default_rng(3).standard_normal(999).astype(np.float32)
+    base = o.global_norm(g)
+    assert o.global_norm(g * np.float32(4.0)) == 4.0 * base
+    assert o.global_norm(g * np.float32(0.125)) == 0.125 * base
+
+
+def pin_clip_closed_forms(o, tmp):
+    """clip(g) has norm <= c, keeps the direction, and is g itself when
+    ||g|| <= c (strict '>' in the threshold test)."""
+    assert o.clip_scale(5.0, 5.0) == 1.0          # ||g|| == c: unchanged
+    assert o.clip_scale(0.0, 1.0) == 1.0          # zero gradient: no division
+    assert o.clip_scale(10.0, 5.0) == 0.5         # [6, 8] with c = 5
+    rng = np.random.default_rng(4)
+    for c in (0.1, 1.0, 30.0):
+        g = rng.standard_normal(500) * rng.uniform(0.01, 5)
+        norm = o.global_norm(g.astype(np.float32))
+        s = o.clip_scale(norm, c)
+        clipped = g.astype(np.float32).astype(np.float64) * s
+        assert np.linalg.norm(clipped) <= c * (1 + 1e-12) or s == 1.0
+        if norm <= c:
+            assert s == 1.0
+        else:
+            assert math.isclose(np.linalg.norm(clipped), c, rel_tol=1e-12)
+        assert s > 0
+
+
+def pin_clipped_vector_step(o, tmp):
+    """First vector step with clipping: m = (1-b1) s g, v = (1-b2) (s g)^2
+    and w = w d - lr sign(g) |s g|/(|s g| + eps), each rounded to float32
+    once, with s = c/||g|| from the Pythagorean vector [30, 40] (norm 50)."""
+    g = np.array([30.0, 40.0, 0.0], np.float32)
+    w = np.array([1.0, -1.0, 0.5], np.float32)
+    m = np.zeros(3, np.float32)
+    v = np.zeros(3, np.float32)
+    lr, wd, c = 0.01, 0.1, 1.0
+    st, norm = o.adamw_clip_step(w, g, m, v, 1, lr, wd, c)
+    assert st == 0 and norm == 50.0
+    s = c / 50.0
+    gh = np.array([30.0 * s, 40.0 * s, 0.0])
+    want_m = (1 - B1) * gh
+    want_v = (1 - B2) * gh * gh
+    upd = np.where(gh != 0, lr * gh / (np.abs(gh) + EPS), 0.0)
+    want_w = np.array([1.0, -1.0, 0.5]) * (1 - lr * wd) - upd
+    for got, want in ((m, want_m), (v, want_v), (w, want_w)):
+        assert np.all(np.abs(got.astype(np.float64) - want)
+                      <= np.abs(want) * 2.0 ** -24 + 1e-30), (got, want)
+
+
+def pin_nonfinite_gradient(o, tmp):
+    """An inf or nan gradient gives a non-finite norm: status ENONFINITE and
+    the state is left bit-for-bit unchanged."""
+    for bad in (np.inf, -np.inf, np.nan):
+        g = np.array([0.1, bad, 0.2], np.float32)
+        w = np.array([1.0, 2.0, 3.0], np.float32)
+        m = np.array([0.1, 0.2, 0.3], np.float32)
+        v = np.array([0.01, 0.02, 0.03], np.float32)
+        before = (w.copy(), m.copy(), v.copy())
+        st, norm = o.adamw_clip_step(w, g, m, v, 3, 0.1, 0.01, 1.0,
+                                     raise_on_error=False)
+        assert st == 6 and not math.isfinite(norm)
+        for a, b in zip((w, m, v), before):
+            assert a.tobytes() == b.tobytes()
+
+
+def pin_step_matches_elements(o, tmp):
+    """The vector step equals, element by element, the scalar update fed the
+    vector's clip factor (the composition norm -> clip -> AdamW)."""
+    rng = np.random.default_rng(5)
+    n = 257
+    w = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 0.2, n).astype(np.float32)
+    m = rng.normal(0, 0.01, n).astype(np.float32)
+    v = np.abs(rng.normal(0, 1e-4, n)).astype(np.float32)
+    w0, m0, v0 = w.copy(), m.copy(), v.copy()
+    st, norm = o.adamw_clip_step(w, g, m, v, 4, 3e-3, 0.01, 1.0)
+    s = o.clip_scale(norm, 1.0)
+    assert s < 1.0
+    ws, ms, vs = o.adamw_at(np.arange(n), w0, g, m0, v0, s, 4, 3e-3, 0.01)
+    assert w.tobytes() == ws.tobytes() and m.tobytes() == ms.tobytes()
+    assert v.tobytes() == vs.tobytes()
+
+
+# --- checkpoint format -----------------------------------------------------
+
+def pin_ckpt_printed_sizes(o, tmp):
+    """8 + 12 n bytes; the pages print 154 MB for 12.8M parameters and about
+    1.44 GB for ~120M."""
+    _, _, _ = read_golden("ckpt_sizes.txt")
+    with open(os.path.join(GOLDEN, "ckpt_sizes.txt")) as f:
+        rows = [l.split() for l in f if l.startswith("params")]
+    for _, n, size, unit, digits in rows:
+        scale = {"MB": 1e6, "GB": 1e9}[unit]
+        got = o.ckpt_size(int(n))
+        assert got == 8 + 12 * int(n)
+        assert round(got / scale, int(digits)) == float(size), (n, got)
+    assert o.ckpt_size(12_800_000) == 153_600_008
+
+
+def pin_pack_layout(o, tmp):
+    """Header = little-endian int32 step then int32 n; then w, m, v as
+    contiguous little-endian float32 regions, in that order."""
+    n = 5
+    w = np.arange(1, 6, dtype=np.float32)
+    m = -np.arange(1, 6, dtype=np.float32)
+    v = np.arange(1, 6, dtype=np.float32) / 8
+    img = o.pack(100, w, m, v)
+    assert img.size == 8 + 12 * n
+    b = img.tobytes()
+    assert struct.unpack("<ii", b[:8]) == (100, n)
+    floats = struct.unpack("<%df" % (3 * n), b[8:])
+    assert list(floats[:n]) == list(w) and list(floats[n:2 * n]) == list(m)
+    assert list(floats[2 * n:]) == list(v)
+
+
+def pin_write_read_roundtrip(o, tmp):
+    """The file is named step_%06d.bin, holds the pack image byte for byte,
+    leaves no .tmp behind and reads back to identical arrays and step."""
+    rng = np.random.default_rng(6)
+    n = 1001
+    w, m, v = (rng.standard_normal(n).astype(np.float32) for _ in range(3))
+    path = o.ckpt_write(str(tmp), 100, w, m, v)
+    assert os.path.basename(path) == "step_000100.bin"
+    assert not os.path.exists(path + ".tmp")
+    with open(path, "rb") as f:
+        data = f.read()
+    assert data == o.pack(100, w, m, v).tobytes()
+    st, step, w2, m2, v2 = o.ckpt_read(path, n)
+    assert st == 0 and step == 100
+    assert w2.tobytes() == w.tobytes() and m2.tobytes() == m.tobytes()
+    assert v2.tobytes() == v.tobytes()
+    p2 = o.ckpt_write(str(tmp), 1234567, w, m, v)
+    assert os.path.basename(p2) == "step_1234567.bin"
+
+
+def pin_read_rejects_bad_files(o, tmp):
+    """Refuse loudly ("Three failure modes"): truncated file, extra bytes,
+    a parameter count that differs from the caller's, a negative header
+    field, a file shorter than the header, a missing file."""
+    n = 16
+    z = np.zeros(n, np.float32)
+    good = o.ckpt_write(str(tmp), 7, z + 1, z + 2, z + 3)
+    data = open(good, "rb").read()
+
+    def case(name, payload):
+        p = os.path.join(str(tmp), name)
+        with open(p, "wb") as f:
+            f.write(payload)
+        return o.ckpt_read(p, n)[0]
+
+    assert case("trunc.bin", data[:-4]) == 4          # ESIZE
+    assert case("extra.bin", data + b"\0") == 4       # ESIZE
+    assert case("short.bin", data[:5]) == 4           # ESIZE
+    assert case("other_n.bin", struct.pack("<ii", 7, n + 1) + data[8:]) == 5  # EMISMATCH
+    assert case("neg_n.bin", struct.pack("<ii", 7, -1) + data[8:]) == 3       # EFORMAT
+    assert case("neg_step.bin", struct.pack("<ii", -2, n) + data[8:]) == 3    # EFORMAT
+    assert o.ckpt_read(os.path.join(str(tmp), "absent.bin"), n)[0] == 2      # EIO
+    assert o.ckpt_read(good, n - 1)[0] == 5
+
+
+def pin_float32_resume_bit_exact(o, tmp):
+    """Saving m and v makes resume bit-equivalent: 3 float32 steps without a
+    break equal 2 steps, write, read, 1 step ("Why save m & v"); resuming
+    from the weights alone does not."""
+    rng = np.random.default_rng(8)
+    n = 333
+    w0 = rng.normal(0, 0.02, n).astype(np.float32)
+    gs = [rng.normal(0, 0.5, n).astype(np.float32) for _ in range(3)]
+
+    def run(w, m, v, t0, steps):
+        for k in steps:
+            o.adamw_clip_step(w, gs[k], m, v, t0 + k + 1, 3e-3, 0.01, 1.0)
+
+    w, m, v = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    run(w, m, v, 0, range(3))
+    w2, m2, v2 = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    run(w2, m2, v2, 0, range(2))
+    path = o.ckpt_write(str(tmp), 2, w2, m2, v2)
+    st, step, w3, m3, v3 = o.ckpt_read(path, n)
+    assert st == 0 and step == 2
+    o.adamw_clip_step(w3, gs[2], m3, v3, step + 1, 3e-3, 0.01, 1.0)
+    assert w3.tobytes() == w.tobytes() and m3.tobytes() == m.tobytes()
+    assert v3.tobytes() == v.tobytes()
+    w4 = w3.copy()
+    w4[:] = o.ckpt_read(path, n)[2]
+    mz, vz = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    o.adamw_clip_step(w4, gs[2], mz, vz, 1, 3e-3, 0.01, 1.0)
+    assert np.max(np.abs(w4.astype(np.float64) - w)) > 1e-4
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
