@@ -1,0 +1,405 @@
+"""Benchmark of the clipped-AdamW optimizer step with resumable checkpoints.
+
+One step = one pass of the whole path over one batch of synthetic input:
+the global-norm reduction, the host bias-correction scalars, the fused
+clip+AdamW kernel and, at the checkpoint cadence (every 100 steps, the
+pages' cadence; at least once per timed region), the device pack, the
+side-stream copy into pinned host memory and the atomic tmp-then-rename
+write of step_NNNNNN.bin.  Inputs (w, g, m, v: 1.77 GB for the 110M list)
+are resident in HBM and larger than L2 before the timed region starts.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--ckpt-every C] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "clip+AdamW params/sec and achieved HBM GB/s vs ~8 TB/s peak, 1 GB300"
+UNIT = "params/s"
+STEP_BYTES = 28      # fused kernel: read w, g, m, v; write w, m, v (float32)
+NORM_BYTES = 4       # norm kernel: read g
+PACK_BYTES = 24      # pack kernel: read w, m, v; write the staging image
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="gpt-110M-list",
+                   help="gpt-110M-list | flat-12.8M | flat-65536 | flat-2^K")
+    p.add_argument("--ckpt-every", type=int, default=100)
+    p.add_argument("--ckpt-dir", default=None)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args(argv)
+
+
+def workload(name):
+    from synthetic import workloads as W
+    if name.startswith("flat-2^"):
+        return W.flat_pow2(int(name.split("^")[1]))
+    return W.WORKLOADS[name]()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel, workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "optimizer_step_resumable_gb300", "csrc", "kernels.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 4 and f[0] == kernel and f[1] == workload_name and f[3] == digest:
+                return float(f[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, index, enabled=True):
+        self.proc = None
+        self.path = None
+        if not enabled or shutil.which("nvidia-smi") is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={index}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv",
+             "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f.read().splitlines()[1:]:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    rows.append((float(c[1].split()[0]), float(c[2].split()[0]),
+                                 float(c[3].split()[0]) if c[3][0].isdigit() else 0.0, c[5:9]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, flag in zip(names, r[3]) if flag == "Active"})
+        busy = [r[0] for r in rows if r[2] > 300.0] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+class OracleTimer:
+    """The oracle's full step (norm, clip, AdamW) on the first S parameters
+    of the workload; single thread, inputs prepared once."""
+
+    def __init__(self, wl, sample=1 << 21):
+        import numpy as np
+
+        import oracle
+        import synthetic
+        self.o = oracle.load()
+        self.wl = wl
+        self.S = S = min(wl.n, sample)
+        self.w = synthetic.weights(wl.seed, n=S)
+        self.g = synthetic.grads(wl.seed, 1, wl.grad_sigma, n=S, outlier_frac=wl.outlier_frac,
+                                 outlier_mult=wl.outlier_mult)
+        self.m = np.zeros(S, np.float32)
+        self.v = np.zeros(S, np.float32)
+        self.t = 1
+        self.total_steps = 0
+        self.total_s = 0.0
+
+    def run(self, seconds):
+        """params/s over repeated steps lasting at least `seconds`."""
+        wl, reps = self.wl, 0
+        t0 = time.perf_counter()
+        while True:
+            self.o.adamw_clip_step(self.w, self.g, self.m, self.v, self.t, wl.lr, wl.wd, wl.clip)
+            reps += 1
+            self.t += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        self.total_steps += reps
+        self.total_s += el
+        return self.S * reps / el
+
+    def describe(self, value):
+        return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"oracle clip+AdamW step (norm, clip, update; double intermediates) "
+                          f"on the first {self.S} parameters of {self.wl.name}, "
+                          f"{self.total_steps} steps in {self.total_s:.1f} s, single thread"}
+
+
+def time_oracle(wl, seconds):
+    timer = OracleTimer(wl)
+    return timer.describe(timer.run(seconds))
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    wl = workload(args.workload)
+    per_step = max(0.25, min(args.cpu_seconds, 90.0 / max(1, args.steps + args.warmup)))
+    timer = OracleTimer(wl)
+    for _ in range(args.warmup):
+        timer.run(per_step / 4)
+    timer.total_steps, timer.total_s = 0, 0.0
+    runs = [timer.run(per_step) for _ in range(args.steps)]
+    value = statistics.median(runs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wl.n / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "n_params": wl.n, "sample_params": timer.S},
+        "cpu_baseline": timer.describe(value),
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import optimizer_step_resumable_gb300 as osr
+    from optimizer_step_resumable_gb300 import build as lib_build
+    from synthetic import device as synth_dev
+
+    lib_build.build()  # no-op when the library is up to date
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload(args.workload)
+    n = wl.n
+    off, num = wl.table()
+    K, W, C = args.steps, max(args.warmup, 0), max(args.ckpt_every, 1)
+
+    w = torch.empty(n, device=dev)
+    g = torch.empty(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    synth_dev.fill_weights(w, wl.seed)
+    synth_dev.fill_grads(g, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
+    ctx = osr.adamw_create(n, off, num)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ckdir = tempfile.mkdtemp(prefix="ckpt_", dir=args.ckpt_dir)
+    torch.cuda.synchronize()
+
+    # checkpoint steps inside the timed region: every C steps, at least one
+    ck_steps = {k for k in range(K) if (k + 1) % C == 0} or {K - 1}
+
+    def checkpoint(step):
+        osr.ckpt_pack(ctx, step, w, m, v, main_stream=main, side_stream=side)
+        osr.ckpt_write(ctx, ckdir)
+
+    t = 1
+    for _ in range(W):
+        osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+        t += 1
+    checkpoint(t - 1)
+    torch.cuda.synchronize()
+
+    # events: per step begin / mid / end around the two kernels; pack events
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for trio in evs:
+        for e in trio:
+            e.record(main)
+    pack_ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for k in ck_steps}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if sampler.proc else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(main)
+    for k in range(K):
+        osr.adamw_record_events(ctx, *evs[k])
+        osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+        if k in ck_steps:
+            a, b = pack_ev[k]
+            a.record(main)
+            osr.ckpt_pack(ctx, t, w, m, v, main_stream=main, side_stream=side)
+            b.record(main)
+            osr.ckpt_write(ctx, ckdir)
+        t += 1
+    end.record(main)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
+    step_ms = [tr[1].elapsed_time(tr[2]) for tr in evs]
+    norm_ms = [tr[0].elapsed_time(tr[1]) for tr in evs]
+    pack_ms = [a.elapsed_time(b) for a, b in pack_ev.values()]
+    norm_val, scale = osr.adamw_last_norm(ctx)
+
+    # end to end through the public API: g copied from pinned host memory each
+    # step, the norm read back each step, checkpoints at the same cadence
+    e2e = None
+    if not args.no_e2e:
+        g_host = g.cpu().pin_memory()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(main)
+        for k in range(K):
+            g.copy_(g_host, non_blocking=True)
+            osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+            osr.adamw_last_norm(ctx)
+            if k in ck_steps:
+                checkpoint(t)
+            t += 1
+        e_end.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
+        e2e = {"value": world * n * K / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": 4 * n,
+               "d2h_bytes_per_step": 8 + (len(ck_steps) * (8 + 12 * n)) / K}
+
+    ctx.close()
+    shutil.rmtree(ckdir, ignore_errors=True)
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    avg_step = statistics.mean(step_ms)
+    achieved = STEP_BYTES * n / (avg_step / 1e3) / 1e9
+    traffic = traffic_record("k_clip_adamw", wl.name)
+    value = world * n * K / (elapsed_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": wl.name, "n_params": n, "tensors": len(off),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "ckpt_every": C, "ckpts_timed": len(ck_steps),
+            "ckpt_bytes": 8 + 12 * n,
+            "l2": f"inputs larger than L2: w, g, m, v = {16 * n / 1e9:.2f} GB",
+            "lr": wl.lr, "wd": wl.wd, "clip": wl.clip, "grad_norm": norm_val,
+            "clip_scale": scale,
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "k_clip_adamw", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+            "bytes_per_launch": STEP_BYTES * n, "traffic": traffic,
+        },
+        "kernels_ms": {
+            "k_grad_norm": {"avg": statistics.mean(norm_ms), "min": min(norm_ms),
+                            "GB/s": NORM_BYTES * n / (statistics.mean(norm_ms) / 1e3) / 1e9},
+            "k_clip_adamw": {"avg": avg_step, "min": min(step_ms), "GB/s": achieved},
+            "k_ckpt_pack": {"avg": statistics.mean(pack_ms) if pack_ms else None,
+                            "GB/s": (PACK_BYTES * n / (statistics.mean(pack_ms) / 1e3) / 1e9)
+                            if pack_ms else None},
+        },
+        "step_only": {"ms": statistics.mean(s + r for s, r in zip(step_ms, norm_ms)),
+                      "GB/s": (STEP_BYTES + NORM_BYTES) * n /
+                      (statistics.mean(s + r for s, r in zip(step_ms, norm_ms)) / 1e3) / 1e9},
+        "gpu_launches": 2 * K + len(ck_steps),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

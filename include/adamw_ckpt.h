@@ -1,0 +1,222 @@
+/*
+ * adamw_ckpt.h -- C ABI of the GB300 (sm_103a) clipped-AdamW optimizer step
+ * and of the step_NNNNNN.bin checkpoint.
+ *
+ * The library updates a flat float32 training state (weights w, gradient g,
+ * Adam moments m and v, n parameters, all resident in GPU memory) once per
+ * training step, and packs / writes / reads that state as one checkpoint
+ * file.  Sources, cited by page title and section:
+ *
+ *  [T] "Training as a Recoverable State Transition" (aihero.club, Language
+ *      Models from Scratch), section "The Exact Targets of Clipping and AdamW"
+ *      -- global L2 clip and AdamW with bias correction and decoupled weight
+ *      decay; section "The Checkpoint Contract and a Real Recovery Test" --
+ *      save after a complete optimizer step, t counts real updates.
+ *  [C] "Grow a Language Model: Checkpoints" (unhomeschool.com), sections
+ *      "Format", "Region by region", "Total size", "Why save m & v" -- the
+ *      file layout [int32 step][int32 n][n f32 w][n f32 m][n f32 v].
+ *  [B] "Grow a Language Model: Backprop" (unhomeschool.com), sections
+ *      "Optimizer state" and "Signals & checkpoints" -- w, g, m, v are one
+ *      buffer each, allocated once at start-up; the clip kernels
+ *      k_grad_norm_partial / k_grad_norm_final / k_grad_scale.
+ *  [S] "Checkpoint and Sharded Resume" (AI Engineering from Scratch, phase
+ *      19 lesson 80), sections "Atomic write" and "Three failure modes".
+ *
+ * Conventions for every entry point:
+ *  - Return value: ADAMW_OK (0) or a negative ADAMW_E* status; a failing
+ *    call leaves a one-line explanation in adamw_last_error() (per thread).
+ *  - Device pointers (d_*) point into memory of the device that was current
+ *    when the context was created; each holds n float32 values laid out in
+ *    the flat parameter order of the offset table.  The caller owns them.
+ *    16-byte aligned pointers take the vectorised path; other alignments
+ *    are accepted and take a scalar path.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on that stream unless stated.
+ *  - The context owns all scratch (device, pinned host); nothing is
+ *    allocated after adamw_create.
+ *  - A context is not thread-safe: one host thread drives it at a time.
+ */
+#ifndef ADAMW_CKPT_H
+#define ADAMW_CKPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ADAMW_API __attribute__((visibility("default")))
+#else
+#define ADAMW_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define ADAMW_OK 0
+#define ADAMW_EINVAL (-1)     /* bad argument: null pointer, size, t < 1 ... */
+#define ADAMW_ECUDA (-2)      /* a CUDA runtime call or kernel launch failed */
+#define ADAMW_EIO (-3)        /* open/read/write/fsync/rename failed         */
+#define ADAMW_EFORMAT (-4)    /* checkpoint header impossible (step/n < 0)   */
+#define ADAMW_ESIZE (-5)      /* file size is not 8 + 12 n, or truncated     */
+#define ADAMW_EMISMATCH (-6)  /* n in the file differs from the context's n  */
+#define ADAMW_ENONFINITE (-7) /* gradient norm inf/nan: update was skipped   */
+#define ADAMW_ESTATE (-8)     /* call out of order (e.g. write with no pack) */
+
+/* adamw_create flags. */
+#define ADAMW_CREATE_NO_CKPT 1 /* do not allocate the checkpoint staging    */
+
+typedef struct adamw_ctx adamw_ctx;
+
+/*
+ * Creates a context for a flat state of n_params float32 values split into
+ * n_tensors tensors: tensor k occupies [offsets[k], offsets[k] + numels[k]).
+ * Flat order per [C] "Region by region": embeddings, then each layer, then
+ * the head.  The table must be sorted, contiguous, without gaps or overlap,
+ * cover exactly [0, n_params), and every numel must be > 0; n_params must be
+ * in [1, 2^31 - 1] (it is stored as an int32 in the checkpoint header).  The
+ * table is copied.  n_tensors = 0 with NULL offsets and numels means one flat
+ * tensor of n_params values.
+ *
+ * Allocates, once ([B] "Optimizer state": every buffer at start-up): the
+ * norm-reduction scratch, a pinned host mirror of the norm result and,
+ * unless ADAMW_CREATE_NO_CKPT is set, a device staging image and a pinned
+ * host image of 8 + 12 n bytes each for the checkpoint.  Uses the current
+ * CUDA device.  AdamW hyperparameters start at beta1 = 0.9,
+ * beta2 = 0.999, eps = 1e-8 ([T]).  On failure *out is set to NULL.
+ */
+ADAMW_API int adamw_create(int64_t n_params, const int64_t* offsets,
+                 const int64_t* numels, int32_t n_tensors, int32_t flags,
+                 adamw_ctx** out);
+
+/* Frees everything the context owns; waits for its pending copies first.
+ * NULL is accepted. */
+ADAMW_API int adamw_destroy(adamw_ctx* ctx);
+
+/* Replaces beta1, beta2 (each in [0, 1)) and eps (>= 0). */
+ADAMW_API int adamw_set_hparams(adamw_ctx* ctx, double beta1, double beta2, double eps);
+
+/* Number of parameters and tensors of the context. */
+ADAMW_API int64_t adamw_num_params(const adamw_ctx* ctx);
+ADAMW_API int32_t adamw_num_tensors(const adamw_ctx* ctx);
+
+/*
+ * Global L2 norm of the gradient d_g[0..n) ([T]: all gradients joined into
+ * one vector g, ||g||_2).  Two-level deterministic reduction: fixed per-block
+ * partial sums of squares (float32 squares summed in short runs, flushed
+ * into double), then one fixed-order double sum; bit-identical from run to
+ * run for a given n.  If h_norm is not NULL the call waits for the stream
+ * and stores the norm there (double); otherwise it returns at once and the
+ * result stays in the context (adamw_last_norm).  Returns ADAMW_ENONFINITE
+ * (with *h_norm = inf or nan) when waited for and the norm is not finite.
+ */
+ADAMW_API int grad_global_norm(adamw_ctx* ctx, const float* d_g, double* h_norm,
+                     void* stream);
+
+/*
+ * One optimizer step, in place on d_w, d_m, d_v ([T]):
+ *   norm = ||g||_2;  s = (norm > clip) ? clip / norm : 1
+ *   g_hat = s g;  m = beta1 m + (1 - beta1) g_hat;
+ *   v = beta2 v + (1 - beta2) g_hat^2
+ *   w = w (1 - lr wd) - lr m_hat / (sqrt(v_hat) + eps),
+ *   m_hat = m / (1 - beta1^t),  v_hat = v / (1 - beta2^t).
+ * t >= 1 is the 1-based index of this update (t counts real optimizer
+ * updates only).  clip > 0 (INFINITY disables clipping); lr, wd >= 0.
+ * d_g is read only.  The bias-correction scalars are computed on the host in
+ * double.  Two kernels on `stream`: the norm reduction, then the fused
+ * clip-scale + AdamW pass that reads w, g, m, v once and writes w, m, v
+ * once.  If the norm is not finite the second kernel leaves w, m, v
+ * untouched; the call itself does not wait, so that outcome is reported by
+ * adamw_last_norm().  Decay applies to every parameter.
+ */
+ADAMW_API int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m,
+                    float* d_v, int32_t t, double lr, double wd, double clip,
+                    void* stream);
+
+/*
+ * Waits for the last norm reduction launched on this context (by
+ * grad_global_norm or adamw_clip_step) and reports it: *norm_out (may be
+ * NULL) receives ||g||_2 in double, *scale_out (may be NULL) the clip factor
+ * that step applied.  Returns ADAMW_ENONFINITE if the norm was inf/nan (the
+ * step, if any, was skipped), ADAMW_ESTATE if no reduction ran yet.
+ */
+ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out);
+
+/*
+ * Instrumentation: the next adamw_clip_step on this context records the given
+ * events (cudaEvent_t passed as void*; NULL entries skipped) on its stream:
+ * ev_begin before the norm kernel, ev_mid between the norm and the fused
+ * kernel, ev_end after the fused kernel.  They apply to that one call only.
+ * Used to time each kernel inside a longer timed region.
+ */
+ADAMW_API int adamw_record_events(adamw_ctx* ctx, void* ev_begin, void* ev_mid,
+                                  void* ev_end);
+
+/*
+ * Checkpoint, part 1 ([C] "Format"; [T] "save after a complete optimizer
+ * step"): a kernel on main_stream packs [int32 step][int32 n][w][m][v] into
+ * the context's device staging image (8 + 12 n bytes, little-endian), then
+ * side_stream copies that image into the context's pinned host image.  The
+ * caller may launch the next step on main_stream right away: the pack reads
+ * w, m, v before it, and the copy reads only the staging image.  A later
+ * pack waits for the previous copy.  side_stream may equal main_stream.
+ * step is the number of completed updates (>= 0); resume continues with
+ * t = step + 1.  ADAMW_ESTATE if the context has no staging.
+ */
+ADAMW_API int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w,
+              const float* d_m, const float* d_v, void* main_stream,
+              void* side_stream);
+
+/*
+ * Checkpoint, part 2 ([S] "Atomic write"): waits for the copy started by
+ * the last ckpt_pack, writes the image to <dir>/step_%06d.bin.tmp, fsyncs
+ * it, renames it to <dir>/step_%06d.bin and fsyncs dir.  A crash before the
+ * rename leaves any previous file of that name intact.  The final path is
+ * copied to path_out (may be NULL) if it fits in path_cap bytes.
+ * ADAMW_ESTATE if there is no packed image; ADAMW_EIO on any file error
+ * (the .tmp file is removed).  Blocks the calling host thread.
+ */
+ADAMW_API int ckpt_write(adamw_ctx* ctx, const char* dir, char* path_out,
+               size_t path_cap);
+
+/*
+ * Resume ([C] "Why save m & v"; [S] "Three failure modes"): opens path,
+ * checks that the header is readable, step >= 0, n == the context's n and
+ * that the file holds exactly 8 + 12 n bytes; only then reads it into the
+ * pinned image and copies w, m, v to d_w, d_m, d_v on `stream`, and waits
+ * for those copies.  *step_out receives the stored step.  On any failure
+ * the device arrays are not modified.  Errors: ADAMW_EIO (cannot open or
+ * read), ADAMW_ESIZE, ADAMW_EFORMAT, ADAMW_EMISMATCH.
+ */
+ADAMW_API int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out,
+              float* d_w, float* d_m, float* d_v, void* stream);
+
+/*
+ * Host-only helpers (no GPU needed).
+ *
+ * ckpt_file_size: 8 + 12 n ([C] "Total size"); -1 if n is outside
+ * [0, 2^31 - 1].
+ *
+ * ckpt_write_host: the atomic writer of ckpt_write applied to host arrays
+ * h_w, h_m, h_v of n floats (e.g. a state held on the host).
+ *
+ * ckpt_probe: validates a file the way ckpt_read does (header, sign, size)
+ * without reading the arrays; *step_out and *n_out (may be NULL) receive the
+ * header fields.  n_expected < 0 skips the n comparison.
+ */
+ADAMW_API int64_t ckpt_file_size(int64_t n);
+ADAMW_API int ckpt_write_host(const char* dir, int32_t step, int32_t n,
+                    const float* h_w, const float* h_m, const float* h_v,
+                    char* path_out, size_t path_cap);
+ADAMW_API int ckpt_probe(const char* path, int32_t n_expected, int32_t* step_out,
+               int32_t* n_out);
+
+/* Name of a status code, and the last failure's explanation (this thread). */
+ADAMW_API const char* adamw_strerror(int status);
+ADAMW_API const char* adamw_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAMW_CKPT_H */

@@ -1,0 +1,267 @@
+"""GB300-native clipped-AdamW optimizer step and step_NNNNNN.bin checkpoint.
+
+Thin Python binding of the C ABI in ``include/adamw_ckpt.h`` (library
+``liboptstep.so``, built in-tree by ``build.py``).  Functions carry the C
+names; this module only marshals arguments: torch tensors become device
+pointers, torch streams become ``cudaStream_t`` handles, non-zero statuses
+become exceptions.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback, and using any function without the
+built library raises ``LibraryNotBuilt``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(PKG, "liboptstep.so")
+
+OK = 0
+EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9, -1)
+CREATE_NO_CKPT = 1
+
+# ABI: name -> (restype, argtypes)
+_c = ctypes
+_vp = _c.c_void_p
+SIGNATURES = {
+    "adamw_create": (_c.c_int, [_c.c_int64, _vp, _vp, _c.c_int32, _c.c_int32,
+                                _c.POINTER(_vp)]),
+    "adamw_destroy": (_c.c_int, [_vp]),
+    "adamw_set_hparams": (_c.c_int, [_vp, _c.c_double, _c.c_double, _c.c_double]),
+    "adamw_num_params": (_c.c_int64, [_vp]),
+    "adamw_num_tensors": (_c.c_int32, [_vp]),
+    "grad_global_norm": (_c.c_int, [_vp, _vp, _c.POINTER(_c.c_double), _vp]),
+    "adamw_clip_step": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _c.c_int32, _c.c_double,
+                                   _c.c_double, _c.c_double, _vp]),
+    "adamw_last_norm": (_c.c_int, [_vp, _c.POINTER(_c.c_double), _c.POINTER(_c.c_float)]),
+    "adamw_record_events": (_c.c_int, [_vp, _vp, _vp, _vp]),
+    "ckpt_pack": (_c.c_int, [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp]),
+    "ckpt_write": (_c.c_int, [_vp, _c.c_char_p, _c.c_char_p, _c.c_size_t]),
+    "ckpt_read": (_c.c_int, [_vp, _c.c_char_p, _c.POINTER(_c.c_int32), _vp, _vp, _vp, _vp]),
+    "ckpt_file_size": (_c.c_int64, [_c.c_int64]),
+    "ckpt_write_host": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_int32, _vp, _vp, _vp,
+                                   _c.c_char_p, _c.c_size_t]),
+    "ckpt_probe": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.POINTER(_c.c_int32),
+                              _c.POINTER(_c.c_int32)]),
+    "adamw_strerror": (_c.c_char_p, [_c.c_int]),
+    "adamw_last_error": (_c.c_char_p, []),
+}
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class AdamWError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {_strerror(status)}: {detail}")
+        self.status = status
+
+
+class NonFiniteGradient(AdamWError):
+    """The gradient norm was inf or nan; the update was skipped."""
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library(path: str = None) -> ctypes.CDLL:
+    """The loaded C library (loaded once, on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIBRARY
+            if not os.path.exists(p):
+                raise LibraryNotBuilt(
+                    f"{p} is missing: build it with optimizer_step_resumable_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def _strerror(status: int) -> str:
+    return library().adamw_strerror(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        detail = library().adamw_last_error().decode()
+        cls = NonFiniteGradient if status == ENONFINITE else AdamWError
+        raise cls(status, where, detail)
+
+
+def _stream(stream):
+    """cudaStream_t of a torch stream (None: torch's current stream)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev_ptr(t, n: int, name: str) -> int:
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    if t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} elements, context has {n}")
+    return t.data_ptr()
+
+
+class Context:
+    """Owner of one ``adamw_ctx*``; freed by ``adamw_destroy`` or on GC."""
+
+    def __init__(self, handle: int, n: int):
+        self.handle = handle
+        self.n = n
+
+    @property
+    def num_tensors(self) -> int:
+        return library().adamw_num_tensors(self.handle)
+
+    def close(self):
+        if self.handle:
+            library().adamw_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def adamw_create(n_params: int, offsets=None, numels=None, flags: int = 0) -> Context:
+    lib = library()
+    if offsets is None and numels is None:
+        nt, po, pn, keep = 0, None, None, ()
+    else:
+        nt = len(offsets)
+        if len(numels) != nt:
+            raise ValueError("offsets and numels differ in length")
+        po = (ctypes.c_int64 * nt)(*offsets)
+        pn = (ctypes.c_int64 * nt)(*numels)
+        keep = (po, pn)
+    out = ctypes.c_void_p()
+    st = lib.adamw_create(int(n_params), po and ctypes.addressof(po),
+                          pn and ctypes.addressof(pn), nt, int(flags), ctypes.byref(out))
+    del keep
+    _check(st, "adamw_create")
+    return Context(out.value, int(n_params))
+
+
+def adamw_destroy(ctx: Context):
+    ctx.close()
+
+
+def adamw_set_hparams(ctx: Context, beta1: float, beta2: float, eps: float):
+    _check(library().adamw_set_hparams(ctx.handle, beta1, beta2, eps), "adamw_set_hparams")
+
+
+def grad_global_norm(ctx: Context, g, wait: bool = True, stream=None):
+    """||g||_2; with wait=False returns None and leaves it in the context."""
+    out = ctypes.c_double()
+    st = library().grad_global_norm(ctx.handle, _dev_ptr(g, ctx.n, "g"),
+                                    ctypes.byref(out) if wait else None, _stream(stream))
+    _check(st, "grad_global_norm")
+    return out.value if wait else None
+
+
+def adamw_clip_step(ctx: Context, w, g, m, v, t: int, lr: float, wd: float,
+                    clip: float, stream=None):
+    n = ctx.n
+    st = library().adamw_clip_step(ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"),
+                                   _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), int(t),
+                                   float(lr), float(wd), float(clip), _stream(stream))
+    _check(st, "adamw_clip_step")
+
+
+def adamw_last_norm(ctx: Context):
+    """(norm, clip factor) of the last reduction; raises NonFiniteGradient."""
+    norm, scale = ctypes.c_double(), ctypes.c_float()
+    st = library().adamw_last_norm(ctx.handle, ctypes.byref(norm), ctypes.byref(scale))
+    _check(st, "adamw_last_norm")
+    return norm.value, scale.value
+
+
+def adamw_record_events(ctx: Context, ev_begin=None, ev_mid=None, ev_end=None):
+    """The next adamw_clip_step records these torch.cuda.Events (already
+    recorded once, so that they exist) around its two kernels."""
+    h = [e.cuda_event if e is not None else None for e in (ev_begin, ev_mid, ev_end)]
+    _check(library().adamw_record_events(ctx.handle, *h), "adamw_record_events")
+
+
+def ckpt_pack(ctx: Context, step: int, w, m, v, main_stream=None, side_stream=None):
+    n = ctx.n
+    ms = _stream(main_stream)
+    ss = ms if side_stream is None else _stream(side_stream)
+    st = library().ckpt_pack(ctx.handle, int(step), _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"),
+                             _dev_ptr(v, n, "v"), ms, ss)
+    _check(st, "ckpt_pack")
+
+
+def ckpt_write(ctx: Context, directory: str) -> str:
+    buf = ctypes.create_string_buffer(4200)
+    st = library().ckpt_write(ctx.handle, os.fsencode(directory), buf, len(buf))
+    _check(st, "ckpt_write")
+    return buf.value.decode()
+
+
+def ckpt_read(ctx: Context, path: str, w, m, v, stream=None) -> int:
+    n = ctx.n
+    step = ctypes.c_int32(-1)
+    st = library().ckpt_read(ctx.handle, os.fsencode(path), ctypes.byref(step),
+                             _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"),
+                             _stream(stream))
+    _check(st, "ckpt_read")
+    return step.value
+
+
+def ckpt_file_size(n: int) -> int:
+    return library().ckpt_file_size(int(n))
+
+
+def ckpt_write_host(directory: str, step: int, w, m, v) -> str:
+    """Atomic write of host float32 numpy arrays w, m, v."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(a, dtype=np.float32) for a in (w, m, v)]
+    n = arrs[0].size
+    if any(a.size != n for a in arrs):
+        raise ValueError("w, m, v differ in size")
+    buf = ctypes.create_string_buffer(4200)
+    st = library().ckpt_write_host(os.fsencode(directory), int(step), int(n),
+                                   *[a.ctypes.data for a in arrs], buf, len(buf))
+    _check(st, "ckpt_write_host")
+    return buf.value.decode()
+
+
+def ckpt_probe(path: str, n_expected: int = -1):
+    """(step, n) of a valid checkpoint file; raises AdamWError otherwise."""
+    step, n = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    st = library().ckpt_probe(os.fsencode(path), int(n_expected), ctypes.byref(step),
+                              ctypes.byref(n))
+    _check(st, "ckpt_probe")
+    return step.value, n.value
+
+
+def adamw_strerror(status: int) -> str:
+    return _strerror(status)
+
+
+def adamw_last_error() -> str:
+    return library().adamw_last_error().decode()

@@ -1,0 +1,469 @@
+// api.cu -- the C ABI entry points of include/adamw_ckpt.h: the context that
+// owns all scratch, the host-side scalars, the launch sequence of one step,
+// and the checkpoint pack / write / read around the staging images.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+#include <unistd.h>
+
+#include "internal.h"
+
+struct adamw_ctx {
+    int64_t n = 0;
+    std::vector<int64_t> offsets, numels;
+    int device = -1;
+    int sm_count = 0;
+    osr::KernelCaps caps{};
+    double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
+
+    // norm scratch: [NormResult | counter | pad][partials x kNormBlocksMax]
+    unsigned char* d_scratch = nullptr;
+    osr::NormResult* d_res = nullptr;
+    unsigned int* d_counter = nullptr;
+    double* d_partials = nullptr;
+    osr::NormResult* h_res = nullptr;      // pinned, mapped: host view
+    osr::NormResult* h_res_dev = nullptr;  // device view of the same memory
+    cudaEvent_t ev_norm = nullptr;
+    bool norm_launched = false;
+    cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
+
+    // checkpoint staging: image = alloc + 8, so the w region (image + 8)
+    // starts on a 16-byte boundary
+    bool has_ckpt = false;
+    unsigned char* d_image_alloc = nullptr;
+    unsigned char* h_image_alloc = nullptr;
+    cudaEvent_t ev_pack = nullptr, ev_d2h = nullptr;
+    bool packed = false, d2h_pending = false;
+    int32_t packed_step = -1;
+
+    unsigned char* d_image() const { return d_image_alloc + 8; }
+    unsigned char* h_image() const { return h_image_alloc + 8; }
+    size_t image_bytes() const { return size_t(8 + 12 * n); }
+};
+
+namespace {
+
+using osr::fail;
+
+constexpr size_t kScratchHead = 256;  // NormResult + counter, padded
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(ADAMW_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(expr)                                       \
+    do {                                                     \
+        cudaError_t e_ = (expr);                             \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #expr);  \
+    } while (0)
+
+// Makes ctx->device current for the scope of one call and restores the
+// caller's device afterwards.
+class DeviceScope {
+public:
+    explicit DeviceScope(int device)
+    {
+        if (cudaGetDevice(&prev_) != cudaSuccess)
+            prev_ = -1;
+        if (prev_ != device && cudaSetDevice(device) == cudaSuccess)
+            switched_ = true;
+    }
+    ~DeviceScope()
+    {
+        if (switched_ && prev_ >= 0)
+            cudaSetDevice(prev_);
+    }
+
+private:
+    int prev_ = -1;
+    bool switched_ = false;
+};
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_state_ptr(const void* p, const char* name)
+{
+    if (!p)
+        return fail(ADAMW_EINVAL, "%s is NULL", name);
+    if (!aligned4(p))
+        return fail(ADAMW_EINVAL, "%s is not 4-byte aligned", name);
+    return ADAMW_OK;
+}
+
+void free_ctx(adamw_ctx* c)
+{
+    if (!c)
+        return;
+    if (c->device >= 0) {
+        DeviceScope scope(c->device);
+        if (c->ev_d2h && c->d2h_pending)
+            cudaEventSynchronize(c->ev_d2h);
+        if (c->ev_norm && c->norm_launched)
+            cudaEventSynchronize(c->ev_norm);
+        if (c->ev_norm) cudaEventDestroy(c->ev_norm);
+        if (c->ev_pack) cudaEventDestroy(c->ev_pack);
+        if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
+        if (c->d_scratch) cudaFree(c->d_scratch);
+        if (c->h_res) cudaFreeHost(c->h_res);
+        if (c->d_image_alloc) cudaFree(c->d_image_alloc);
+        if (c->h_image_alloc) cudaFreeHost(c->h_image_alloc);
+    }
+    delete c;
+}
+
+int validate_table(int64_t n, const int64_t* offsets, const int64_t* numels, int32_t nt)
+{
+    if (n < 1 || n > INT32_MAX)
+        return fail(ADAMW_EINVAL, "n_params=%lld outside [1, 2^31-1]", (long long)n);
+    if (nt < 0)
+        return fail(ADAMW_EINVAL, "n_tensors=%d is negative", nt);
+    if (nt == 0) {
+        if (offsets || numels)
+            return fail(ADAMW_EINVAL, "n_tensors=0 needs NULL offsets and numels");
+        return ADAMW_OK;
+    }
+    if (!offsets || !numels)
+        return fail(ADAMW_EINVAL, "offset table is NULL");
+    int64_t expect = 0;
+    for (int32_t k = 0; k < nt; ++k) {
+        if (numels[k] <= 0)
+            return fail(ADAMW_EINVAL, "tensor %d has numel %lld", k, (long long)numels[k]);
+        if (offsets[k] != expect)
+            return fail(ADAMW_EINVAL,
+                        "tensor %d starts at %lld, expected %lld (table must be sorted, "
+                        "contiguous, without gaps or overlap)",
+                        k, (long long)offsets[k], (long long)expect);
+        if (numels[k] > n - expect)
+            return fail(ADAMW_EINVAL, "tensor %d ends past n_params", k);
+        expect += numels[k];
+    }
+    if (expect != n)
+        return fail(ADAMW_EINVAL, "tensors cover %lld of %lld parameters", (long long)expect,
+                    (long long)n);
+    return ADAMW_OK;
+}
+
+int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream)
+{
+    const int e = osr::launch_norm(g, c->n, clip, c->d_partials, c->d_counter, c->d_res,
+                                   c->h_res_dev, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(cudaError_t(e), "norm kernel launch");
+    CUDA_TRY(cudaEventRecord(c->ev_norm, static_cast<cudaStream_t>(stream)));
+    c->norm_launched = true;
+    return ADAMW_OK;
+}
+
+int read_norm(adamw_ctx* c, double* norm_out, float* scale_out)
+{
+    if (!c->norm_launched)
+        return fail(ADAMW_ESTATE, "no norm reduction has run on this context");
+    CUDA_TRY(cudaEventSynchronize(c->ev_norm));
+    const volatile osr::NormResult* r = c->h_res;
+    const double norm = r->norm;
+    const float scale = r->scale;
+    const int nonfinite = r->nonfinite;
+    if (norm_out)
+        *norm_out = norm;
+    if (scale_out)
+        *scale_out = scale;
+    if (nonfinite)
+        return fail(ADAMW_ENONFINITE, "gradient norm is %g: the update was skipped", norm);
+    return ADAMW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels,
+                 int32_t n_tensors, int32_t flags, adamw_ctx** out)
+{
+    osr::clear_error();
+    if (!out)
+        return fail(ADAMW_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = validate_table(n_params, offsets, numels, n_tensors);
+    if (rc != ADAMW_OK)
+        return rc;
+    if (flags & ~ADAMW_CREATE_NO_CKPT)
+        return fail(ADAMW_EINVAL, "unknown flags 0x%x", flags);
+
+    adamw_ctx* c = new (std::nothrow) adamw_ctx;
+    if (!c)
+        return fail(ADAMW_EINVAL, "out of host memory");
+    c->n = n_params;
+    if (n_tensors > 0) {
+        c->offsets.assign(offsets, offsets + n_tensors);
+        c->numels.assign(numels, numels + n_tensors);
+    } else {
+        c->offsets.assign(1, 0);
+        c->numels.assign(1, n_params);
+    }
+    auto bail = [&](int status) {
+        free_ctx(c);
+        return status;
+    };
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e != cudaSuccess) {
+        c->device = -1;
+        return bail(cuda_fail(e, "cudaGetDevice"));
+    }
+    if ((e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device)) !=
+        cudaSuccess)
+        return bail(cuda_fail(e, "cudaDeviceGetAttribute"));
+    if (int qe = osr::query_kernel_caps(c->sm_count, &c->caps))
+        return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
+
+    const size_t scratch = kScratchHead + sizeof(double) * osr::kNormBlocksMax;
+    if ((e = cudaMalloc(&c->d_scratch, scratch)) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaMalloc(norm scratch)"));
+    if ((e = cudaMemset(c->d_scratch, 0, scratch)) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaMemset(norm scratch)"));
+    c->d_res = reinterpret_cast<osr::NormResult*>(c->d_scratch);
+    c->d_counter = reinterpret_cast<unsigned int*>(c->d_scratch + sizeof(osr::NormResult));
+    c->d_partials = reinterpret_cast<double*>(c->d_scratch + kScratchHead);
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_res), sizeof(osr::NormResult),
+                           cudaHostAllocMapped)) != cudaSuccess) {
+        c->h_res = nullptr;
+        return bail(cuda_fail(e, "cudaHostAlloc(norm mirror)"));
+    }
+    std::memset(c->h_res, 0, sizeof(osr::NormResult));
+    if ((e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->h_res_dev), c->h_res, 0)) !=
+        cudaSuccess)
+        return bail(cuda_fail(e, "cudaHostGetDevicePointer"));
+    if ((e = cudaEventCreateWithFlags(&c->ev_norm, cudaEventDisableTiming)) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaEventCreate"));
+
+    if (!(flags & ADAMW_CREATE_NO_CKPT)) {
+        const size_t bytes = 16 + size_t(12) * size_t(n_params);
+        if ((e = cudaMalloc(&c->d_image_alloc, bytes)) != cudaSuccess) {
+            c->d_image_alloc = nullptr;
+            return bail(cuda_fail(e, "cudaMalloc(checkpoint staging)"));
+        }
+        if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_image_alloc), bytes,
+                               cudaHostAllocDefault)) != cudaSuccess) {
+            c->h_image_alloc = nullptr;
+            return bail(cuda_fail(e, "cudaHostAlloc(checkpoint image)"));
+        }
+        if ((e = cudaEventCreateWithFlags(&c->ev_pack, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->ev_d2h, cudaEventDisableTiming)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaEventCreate"));
+        c->has_ckpt = true;
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess)
+        return bail(cuda_fail(e, "cudaDeviceSynchronize"));
+    *out = c;
+    return ADAMW_OK;
+}
+
+int adamw_destroy(adamw_ctx* ctx)
+{
+    osr::clear_error();
+    free_ctx(ctx);
+    return ADAMW_OK;
+}
+
+int adamw_set_hparams(adamw_ctx* ctx, double beta1, double beta2, double eps)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0) ||
+        !(eps >= 0.0 && std::isfinite(eps)))
+        return fail(ADAMW_EINVAL, "need 0 <= beta1, beta2 < 1 and finite eps >= 0");
+    ctx->beta1 = beta1;
+    ctx->beta2 = beta2;
+    ctx->eps = eps;
+    return ADAMW_OK;
+}
+
+int64_t adamw_num_params(const adamw_ctx* ctx) { return ctx ? ctx->n : -1; }
+
+int32_t adamw_num_tensors(const adamw_ctx* ctx)
+{
+    return ctx ? int32_t(ctx->offsets.size()) : -1;
+}
+
+int grad_global_norm(adamw_ctx* ctx, const float* d_g, double* h_norm, void* stream)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    int rc = check_state_ptr(d_g, "d_g");
+    if (rc != ADAMW_OK)
+        return rc;
+    DeviceScope scope(ctx->device);
+    rc = launch_norm_on(ctx, d_g, INFINITY, stream);
+    if (rc != ADAMW_OK || !h_norm)
+        return rc;
+    return read_norm(ctx, h_norm, nullptr);
+}
+
+int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, float* d_v,
+                    int32_t t, double lr, double wd, double clip, void* stream)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    int rc;
+    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_g, "d_g")) ||
+        (rc = check_state_ptr(d_m, "d_m")) || (rc = check_state_ptr(d_v, "d_v")))
+        return rc;
+    if (t < 1)
+        return fail(ADAMW_EINVAL, "t=%d: the first update has t = 1", t);
+    if (!(lr >= 0.0 && std::isfinite(lr)) || !(wd >= 0.0 && std::isfinite(wd)))
+        return fail(ADAMW_EINVAL, "lr=%g wd=%g must be finite and >= 0", lr, wd);
+    if (!(clip > 0.0))
+        return fail(ADAMW_EINVAL, "clip=%g must be > 0 (INFINITY disables clipping)", clip);
+
+    // Bias-correction and decay scalars, in double on the host, rounded to
+    // float once.
+    const double bc1 = 1.0 - std::pow(ctx->beta1, double(t));
+    const double bc2 = 1.0 - std::pow(ctx->beta2, double(t));
+    osr::StepScalars k;
+    k.beta1 = float(ctx->beta1);
+    k.omb1 = float(1.0 - ctx->beta1);
+    k.beta2 = float(ctx->beta2);
+    k.omb2 = float(1.0 - ctx->beta2);
+    k.eps = float(ctx->eps);
+    k.step_size = float(lr / bc1);
+    k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+    k.decay = float(1.0 - lr * wd);
+
+    DeviceScope scope(ctx->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaEvent_t prof[3] = {ctx->prof[0], ctx->prof[1], ctx->prof[2]};
+    ctx->prof[0] = ctx->prof[1] = ctx->prof[2] = nullptr;
+    if (prof[0])
+        CUDA_TRY(cudaEventRecord(prof[0], st));
+    rc = launch_norm_on(ctx, d_g, clip, stream);
+    if (rc != ADAMW_OK)
+        return rc;
+    if (prof[1])
+        CUDA_TRY(cudaEventRecord(prof[1], st));
+    const int e = osr::launch_adamw(d_w, d_g, d_m, d_v, ctx->n, k, ctx->d_res, ctx->caps, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(cudaError_t(e), "clip+AdamW kernel launch");
+    if (prof[2])
+        CUDA_TRY(cudaEventRecord(prof[2], st));
+    return ADAMW_OK;
+}
+
+int adamw_record_events(adamw_ctx* ctx, void* ev_begin, void* ev_mid, void* ev_end)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    ctx->prof[0] = static_cast<cudaEvent_t>(ev_begin);
+    ctx->prof[1] = static_cast<cudaEvent_t>(ev_mid);
+    ctx->prof[2] = static_cast<cudaEvent_t>(ev_end);
+    return ADAMW_OK;
+}
+
+int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    DeviceScope scope(ctx->device);
+    return read_norm(ctx, norm_out, scale_out);
+}
+
+int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
+              const float* d_v, void* main_stream, void* side_stream)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    if (!ctx->has_ckpt)
+        return fail(ADAMW_ESTATE, "context was created without checkpoint staging");
+    int rc;
+    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_m, "d_m")) ||
+        (rc = check_state_ptr(d_v, "d_v")))
+        return rc;
+    if (step < 0)
+        return fail(ADAMW_EINVAL, "step=%d is negative", step);
+    DeviceScope scope(ctx->device);
+    cudaStream_t mainst = static_cast<cudaStream_t>(main_stream);
+    cudaStream_t side = static_cast<cudaStream_t>(side_stream);
+    // The staging image may still be read by the previous copy.
+    if (ctx->d2h_pending)
+        CUDA_TRY(cudaStreamWaitEvent(mainst, ctx->ev_d2h, 0));
+    const int e = osr::launch_pack(d_w, d_m, d_v, ctx->n, step, ctx->d_image(), ctx->caps,
+                                   main_stream);
+    if (e != cudaSuccess)
+        return cuda_fail(cudaError_t(e), "pack kernel launch");
+    CUDA_TRY(cudaEventRecord(ctx->ev_pack, mainst));
+    if (side != mainst)
+        CUDA_TRY(cudaStreamWaitEvent(side, ctx->ev_pack, 0));
+    CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_image(), ctx->image_bytes(),
+                             cudaMemcpyDeviceToHost, side));
+    CUDA_TRY(cudaEventRecord(ctx->ev_d2h, side));
+    ctx->packed = true;
+    ctx->d2h_pending = true;
+    ctx->packed_step = step;
+    return ADAMW_OK;
+}
+
+int ckpt_write(adamw_ctx* ctx, const char* dir, char* path_out, size_t path_cap)
+{
+    osr::clear_error();
+    if (!ctx || !dir)
+        return fail(ADAMW_EINVAL, "ctx or dir is NULL");
+    if (!ctx->packed)
+        return fail(ADAMW_ESTATE, "no packed checkpoint: call ckpt_pack first");
+    {
+        DeviceScope scope(ctx->device);
+        CUDA_TRY(cudaEventSynchronize(ctx->ev_d2h));
+    }
+    ctx->d2h_pending = false;
+    const osr::IoPiece piece{ctx->h_image(), ctx->image_bytes()};
+    return osr::write_file_atomic(dir, ctx->packed_step, &piece, 1, path_out, path_cap);
+}
+
+int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out, float* d_w, float* d_m,
+              float* d_v, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !path)
+        return fail(ADAMW_EINVAL, "ctx or path is NULL");
+    if (!ctx->has_ckpt)
+        return fail(ADAMW_ESTATE, "context was created without checkpoint staging");
+    int rc;
+    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_m, "d_m")) ||
+        (rc = check_state_ptr(d_v, "d_v")))
+        return rc;
+    DeviceScope scope(ctx->device);
+    if (ctx->d2h_pending) {
+        CUDA_TRY(cudaEventSynchronize(ctx->ev_d2h));
+        ctx->d2h_pending = false;
+    }
+    int32_t step = -1;
+    int fd = -1;
+    rc = osr::open_validated(path, int32_t(ctx->n), &step, nullptr, &fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    ctx->packed = false;  // the pinned image is about to hold the file instead
+    const size_t bytes = size_t(ctx->n) * 4u;
+    unsigned char* body = ctx->h_image() + 8;
+    rc = osr::read_exact(fd, body, 3 * bytes, path);
+    ::close(fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaMemcpyAsync(d_w, body, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(d_m, body + bytes, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(d_v, body + 2 * bytes, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (step_out)
+        *step_out = step;
+    return ADAMW_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,254 @@
+// ckpt_io.cpp -- host side of the step_NNNNNN.bin checkpoint: the atomic
+// writer and the validating reader.  Plain POSIX, no CUDA.
+//
+// Format ("Grow a Language Model: Checkpoints", unhomeschool.com, sections
+// "Format" and "Total size"): [int32 step][int32 n][n f32 w][n f32 m]
+// [n f32 v], 8 + 12 n bytes, no other metadata; little-endian.
+// Atomicity ("Checkpoint and Sharded Resume", AI Engineering from Scratch
+// lesson 80, section "Atomic write"): write <name>.tmp, fsync, rename over
+// <name>, fsync the directory.  Refusal of bad files (same page, "Three
+// failure modes"): header, sign, parameter count and exact size are checked
+// before any byte of the arrays is used.
+#include <cerrno>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <fcntl.h>
+#include <sys/stat.h>
+#include <sys/uio.h>
+#include <unistd.h>
+
+#include "internal.h"
+
+namespace osr {
+
+namespace {
+thread_local char g_last_error[512];
+
+bool little_endian_host()
+{
+    const uint32_t one = 1;
+    unsigned char b;
+    std::memcpy(&b, &one, 1);
+    return b == 1;
+}
+
+void put_le32(unsigned char* p, uint32_t x)
+{
+    for (int i = 0; i < 4; ++i)
+        p[i] = static_cast<unsigned char>((x >> (8 * i)) & 0xffu);
+}
+
+uint32_t get_le32(const unsigned char* p)
+{
+    return uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16) |
+           (uint32_t(p[3]) << 24);
+}
+
+int write_exact(int fd, const void* src, size_t bytes, const char* path)
+{
+    const unsigned char* p = static_cast<const unsigned char*>(src);
+    while (bytes > 0) {
+        // Linux moves at most ~2 GiB per write(); loop on short writes.
+        const size_t want = bytes > (size_t(1) << 30) ? (size_t(1) << 30) : bytes;
+        const ssize_t got = ::write(fd, p, want);
+        if (got < 0) {
+            if (errno == EINTR)
+                continue;
+            return fail(ADAMW_EIO, "write %s: %s", path, std::strerror(errno));
+        }
+        p += got;
+        bytes -= size_t(got);
+    }
+    return ADAMW_OK;
+}
+}  // namespace
+
+int fail(int status, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+void clear_error() { g_last_error[0] = '\0'; }
+
+const char* last_error_text() { return g_last_error; }
+
+int read_exact(int fd, void* dst, size_t bytes, const char* path)
+{
+    unsigned char* p = static_cast<unsigned char*>(dst);
+    while (bytes > 0) {
+        const size_t want = bytes > (size_t(1) << 30) ? (size_t(1) << 30) : bytes;
+        const ssize_t got = ::read(fd, p, want);
+        if (got < 0) {
+            if (errno == EINTR)
+                continue;
+            return fail(ADAMW_EIO, "read %s: %s", path, std::strerror(errno));
+        }
+        if (got == 0)
+            return fail(ADAMW_ESIZE, "%s: file ended early", path);
+        p += got;
+        bytes -= size_t(got);
+    }
+    return ADAMW_OK;
+}
+
+int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
+                      int npieces, char* path_out, size_t path_cap)
+{
+    if (!dir || step < 0)
+        return fail(ADAMW_EINVAL, "ckpt write: null directory or negative step");
+    if (!little_endian_host())
+        return fail(ADAMW_EINVAL, "ckpt write: big-endian host not supported");
+    char final_path[4096], tmp_path[4112];
+    const int len = std::snprintf(final_path, sizeof final_path, "%s/step_%06d.bin",
+                                  dir, int(step));
+    if (len < 0 || size_t(len) >= sizeof final_path)
+        return fail(ADAMW_EINVAL, "ckpt write: directory name too long");
+    std::snprintf(tmp_path, sizeof tmp_path, "%s.tmp", final_path);
+
+    const int fd = ::open(tmp_path, O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC, 0644);
+    if (fd < 0)
+        return fail(ADAMW_EIO, "open %s: %s", tmp_path, std::strerror(errno));
+    int rc = ADAMW_OK;
+    for (int i = 0; i < npieces && rc == ADAMW_OK; ++i)
+        rc = write_exact(fd, pieces[i].data, pieces[i].bytes, tmp_path);
+    if (rc == ADAMW_OK && ::fsync(fd) != 0)
+        rc = fail(ADAMW_EIO, "fsync %s: %s", tmp_path, std::strerror(errno));
+    if (::close(fd) != 0 && rc == ADAMW_OK)
+        rc = fail(ADAMW_EIO, "close %s: %s", tmp_path, std::strerror(errno));
+    if (rc != ADAMW_OK) {
+        ::unlink(tmp_path);
+        return rc;
+    }
+    if (::rename(tmp_path, final_path) != 0) {
+        rc = fail(ADAMW_EIO, "rename %s: %s", tmp_path, std::strerror(errno));
+        ::unlink(tmp_path);
+        return rc;
+    }
+    const int dfd = ::open(dir, O_RDONLY | O_CLOEXEC);
+    if (dfd >= 0) {
+        ::fsync(dfd);
+        ::close(dfd);
+    }
+    if (path_out && path_cap > 0) {
+        if (size_t(len) + 1 > path_cap)
+            return fail(ADAMW_EINVAL, "ckpt write: path buffer too small (file written)");
+        std::memcpy(path_out, final_path, size_t(len) + 1);
+    }
+    return ADAMW_OK;
+}
+
+int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
+                   int32_t* n_out, int* fd_out)
+{
+    *fd_out = -1;
+    if (!path)
+        return fail(ADAMW_EINVAL, "ckpt read: null path");
+    if (!little_endian_host())
+        return fail(ADAMW_EINVAL, "ckpt read: big-endian host not supported");
+    const int fd = ::open(path, O_RDONLY | O_CLOEXEC);
+    if (fd < 0)
+        return fail(ADAMW_EIO, "open %s: %s", path, std::strerror(errno));
+    struct stat st;
+    if (::fstat(fd, &st) != 0) {
+        const int e = errno;
+        ::close(fd);
+        return fail(ADAMW_EIO, "stat %s: %s", path, std::strerror(e));
+    }
+    unsigned char header[8];
+    if (st.st_size < 8) {
+        ::close(fd);
+        return fail(ADAMW_ESIZE, "%s: %lld bytes, shorter than the 8-byte header", path,
+                    (long long)st.st_size);
+    }
+    int rc = read_exact(fd, header, 8, path);
+    if (rc != ADAMW_OK) {
+        ::close(fd);
+        return rc;
+    }
+    const int32_t step = int32_t(get_le32(header));
+    const int32_t n = int32_t(get_le32(header + 4));
+    if (step < 0 || n < 0) {
+        ::close(fd);
+        return fail(ADAMW_EFORMAT, "%s: header step=%d n=%d (negative)", path, step, n);
+    }
+    if (n_expected >= 0 && n != n_expected) {
+        ::close(fd);
+        return fail(ADAMW_EMISMATCH, "%s: holds %d parameters, expected %d", path, n,
+                    n_expected);
+    }
+    const int64_t want = 8 + 12 * int64_t(n);
+    if (int64_t(st.st_size) != want) {
+        ::close(fd);
+        return fail(ADAMW_ESIZE, "%s: %lld bytes, expected 8 + 12 x %d = %lld", path,
+                    (long long)st.st_size, n, (long long)want);
+    }
+    if (step_out)
+        *step_out = step;
+    if (n_out)
+        *n_out = n;
+    *fd_out = fd;
+    return ADAMW_OK;
+}
+
+}  // namespace osr
+
+extern "C" {
+
+int64_t ckpt_file_size(int64_t n)
+{
+    if (n < 0 || n > INT32_MAX)
+        return -1;
+    return 8 + 12 * n;
+}
+
+int ckpt_write_host(const char* dir, int32_t step, int32_t n, const float* h_w,
+                    const float* h_m, const float* h_v, char* path_out,
+                    size_t path_cap)
+{
+    osr::clear_error();
+    if (n < 0 || (n > 0 && (!h_w || !h_m || !h_v)))
+        return osr::fail(ADAMW_EINVAL, "ckpt_write_host: bad n or null array");
+    unsigned char header[8];
+    osr::put_le32(header, uint32_t(step));
+    osr::put_le32(header + 4, uint32_t(n));
+    const size_t bytes = size_t(n) * 4u;
+    const osr::IoPiece pieces[4] = {{header, 8}, {h_w, bytes}, {h_m, bytes}, {h_v, bytes}};
+    return osr::write_file_atomic(dir, step, pieces, 4, path_out, path_cap);
+}
+
+int ckpt_probe(const char* path, int32_t n_expected, int32_t* step_out, int32_t* n_out)
+{
+    osr::clear_error();
+    int fd = -1;
+    const int rc = osr::open_validated(path, n_expected, step_out, n_out, &fd);
+    if (fd >= 0)
+        ::close(fd);
+    return rc;
+}
+
+const char* adamw_strerror(int status)
+{
+    switch (status) {
+    case ADAMW_OK: return "ADAMW_OK";
+    case ADAMW_EINVAL: return "ADAMW_EINVAL: invalid argument";
+    case ADAMW_ECUDA: return "ADAMW_ECUDA: CUDA runtime error";
+    case ADAMW_EIO: return "ADAMW_EIO: file I/O error";
+    case ADAMW_EFORMAT: return "ADAMW_EFORMAT: bad checkpoint header";
+    case ADAMW_ESIZE: return "ADAMW_ESIZE: checkpoint size is not 8 + 12 n";
+    case ADAMW_EMISMATCH: return "ADAMW_EMISMATCH: checkpoint parameter count differs";
+    case ADAMW_ENONFINITE: return "ADAMW_ENONFINITE: gradient norm is not finite";
+    case ADAMW_ESTATE: return "ADAMW_ESTATE: call out of order";
+    default: return "unknown status";
+    }
+}
+
+const char* adamw_last_error(void) { return osr::last_error_text(); }
+
+}  // extern "C"

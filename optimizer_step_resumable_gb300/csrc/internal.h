@@ -1,0 +1,89 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/adamw_ckpt.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "adamw_ckpt.h"
+
+namespace osr {
+
+// ---------------------------------------------------------------------------
+// Error reporting: every failing entry point stores one line per thread.
+// ---------------------------------------------------------------------------
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+void clear_error();
+const char* last_error_text();
+
+// ---------------------------------------------------------------------------
+// Norm reduction result, written by the last block of the norm kernel into
+// device scratch (read by the fused step kernel) and into a pinned, mapped
+// host mirror (read by adamw_last_norm without a copy).
+// ---------------------------------------------------------------------------
+struct NormResult {
+    double sumsq;       // sum of g_i^2 (fixed-order, double)
+    double norm;        // sqrt(sumsq)
+    float scale;        // clip factor: norm > clip ? clip / norm : 1
+    int32_t nonfinite;  // 1 if norm is inf or nan (the step is skipped)
+    uint32_t seq;       // incremented by every reduction (host staleness check)
+    uint32_t pad;
+};
+
+// Per-step scalars, computed on the host in double and rounded to float once.
+struct StepScalars {
+    float beta1, omb1;      // beta1 and 1 - beta1
+    float beta2, omb2;      // beta2 and 1 - beta2
+    float eps;
+    float step_size;        // lr / (1 - beta1^t)
+    float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
+    float decay;            // 1 - lr * wd
+};
+
+// Tunables of the kernels (fixed at compile time; see kernels.cu).
+constexpr int kNormThreads = 256;
+constexpr int kNormVecPerThread = 8;                 // float4 per thread per tile
+constexpr int64_t kNormTileElems = int64_t(kNormThreads) * kNormVecPerThread * 4;
+constexpr int kNormBlocksMax = 1216;                 // 8 x 152 SMs; fixed, not device-derived
+
+// Number of blocks of the norm reduction for n elements: a function of n
+// only, so the reduction order (and hence every bit of the result) is too.
+inline int norm_blocks(int64_t n)
+{
+    int64_t tiles = (n + kNormTileElems - 1) / kNormTileElems;
+    if (tiles < 1) tiles = 1;
+    return tiles > kNormBlocksMax ? kNormBlocksMax : int(tiles);
+}
+
+// Resident-block counts of the grid-stride kernels on this device (their
+// grids are capped there: one wave of persistent blocks).
+struct KernelCaps {
+    int step_vec, step_scalar, pack_vec, pack_scalar;
+};
+
+// Kernel launchers (kernels.cu).  All return cudaError_t as int.
+int query_kernel_caps(int sm_count, KernelCaps* caps);
+int launch_norm(const float* g, int64_t n, double clip, double* partials,
+                unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                void* stream);
+int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
+                 const StepScalars& k, const NormResult* d_res,
+                 const KernelCaps& caps, void* stream);
+int launch_pack(const float* w, const float* m, const float* v, int64_t n,
+                int32_t step, unsigned char* image, const KernelCaps& caps,
+                void* stream);
+
+// Host file I/O (ckpt_io.cpp).
+struct IoPiece {
+    const void* data;
+    size_t bytes;
+};
+int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
+                      int npieces, char* path_out, size_t path_cap);
+// Validates header and size; on success *fd_out is an open descriptor
+// positioned after the header (caller closes it).
+int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
+                   int32_t* n_out, int* fd_out);
+int read_exact(int fd, void* dst, size_t bytes, const char* path);
+
+}  // namespace osr

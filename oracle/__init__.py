@@ -96,6 +96,11 @@ class Oracle:
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
             c.c_double, _f32p, _f32p, _f32p]
         lib.oracle_adamw_at.restype = None
+        lib.oracle_adamw_terms_at.argtypes = [
+            _i64p, c.c_int64, _f32p, _f32p, _f32p, _f32p, c.c_double,
+            c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
+            c.c_double, np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")]
+        lib.oracle_adamw_terms_at.restype = None
         lib.oracle_ckpt_size.argtypes = [c.c_int64]
         lib.oracle_ckpt_size.restype = c.c_int64
         lib.oracle_pack.argtypes = [c.c_int32, c.c_int32, _f32p, _f32p, _f32p, _u8p]
@@ -161,6 +166,19 @@ class Oracle:
                                   float(beta1), float(beta2), float(eps),
                                   *outs)
         return tuple(outs)
+
+    TERMS = ("g_hat", "m", "v", "m_hat", "v_hat", "w_decayed", "update", "w")
+
+    def adamw_terms_at(self, idx, w, g, m, v, s, t, lr, wd, beta1=BETA1,
+                       beta2=BETA2, eps=EPS) -> np.ndarray:
+        """(k, 8) double terms at indices idx, columns as in TERMS."""
+        idx = np.ascontiguousarray(idx, dtype=np.int64)
+        out = np.empty((idx.size, 8), np.float64)
+        self._lib.oracle_adamw_terms_at(idx, idx.size, _f32(w), _f32(g), _f32(m),
+                                        _f32(v), float(s), int(t), float(lr),
+                                        float(wd), float(beta1), float(beta2),
+                                        float(eps), out)
+        return out
 
     # --- checkpoint ------------------------------------------------------
     def ckpt_size(self, n: int) -> int:

@@ -178,6 +178,32 @@ void oracle_adamw_at(const int64_t* idx, int64_t k, const float* w,
     }
 }
 
+/* All eight double terms of the update at chosen indices (row j of out holds
+ * g_hat, m, v, m_hat, v_hat, w_decayed, update, w for idx[j]).  The tests
+ * use them as the magnitudes that a float32 result may differ by, relative
+ * to: the new weight is a difference of two terms that can cancel. */
+void oracle_adamw_terms_at(const int64_t* idx, int64_t k, const float* w,
+                           const float* g, const float* m, const float* v,
+                           double s, int32_t t, double lr, double wd,
+                           double beta1, double beta2, double eps, double* out)
+{
+    for (int64_t j = 0; j < k; ++j) {
+        int64_t i = idx[j];
+        oracle_terms r;
+        oracle_adamw_element((double)w[i], (double)g[i], (double)m[i],
+                             (double)v[i], s, t, lr, wd, beta1, beta2, eps, &r);
+        double* o = out + 8 * j;
+        o[0] = r.g_hat;
+        o[1] = r.m;
+        o[2] = r.v;
+        o[3] = r.m_hat;
+        o[4] = r.v_hat;
+        o[5] = r.w_decayed;
+        o[6] = r.update;
+        o[7] = r.w;
+    }
+}
+
 /* ------------------------------------------------------------------------
  * The step_NNNNNN.bin image.  [C] "Format" / "Region by region" /
  * "Total size": five contiguous regions

@@ -19,3 +19,12 @@ def pytest_configure(config):
 def oracle():
     import oracle as oracle_pkg
     return oracle_pkg.load()
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The product's C library, built in-tree if missing or stale."""
+    from optimizer_step_resumable_gb300 import build as lib_build
+    lib_build.build()
+    import optimizer_step_resumable_gb300 as osr
+    return osr.library()
