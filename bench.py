@@ -38,6 +38,7 @@ STEP_BYTES = 28      # fused kernel: read w, g, m, v; write w, m, v (float32)
 NORM_BYTES = 4       # norm kernel: read g
 PACK_BYTES = 24      # pack kernel: read w, m, v; write the staging image
 FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {"k_clip_adamw": "step.cu", "k_grad_norm": "norm.cu", "k_ckpt_pack": "pack.cu"}
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -81,7 +82,7 @@ def traffic_record(kernel, workload_name):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "optimizer_step_resumable_gb300", "csrc", "kernels.cu")
+    src = os.path.join(ROOT, "optimizer_step_resumable_gb300", "csrc", KERNEL_SOURCES[kernel])
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         for line in open(path):

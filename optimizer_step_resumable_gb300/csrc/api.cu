@@ -217,7 +217,9 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
     if ((e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device)) !=
         cudaSuccess)
         return bail(cuda_fail(e, "cudaDeviceGetAttribute"));
-    if (int qe = osr::query_kernel_caps(c->sm_count, &c->caps))
+    if (int qe = osr::query_step_caps(c->sm_count, &c->caps))
+        return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
+    if (int qe = osr::query_pack_caps(c->sm_count, &c->caps))
         return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
 
     const size_t scratch = kScratchHead + sizeof(double) * osr::kNormBlocksMax;

@@ -44,7 +44,10 @@ struct StepScalars {
 constexpr int kNormThreads = 256;
 constexpr int kNormVecPerThread = 8;                 // float4 per thread per tile
 constexpr int64_t kNormTileElems = int64_t(kNormThreads) * kNormVecPerThread * 4;
-constexpr int kNormBlocksMax = 1216;                 // 8 x 152 SMs; fixed, not device-derived
+// At most 608 = 4 x 152 blocks: four 256-thread blocks of the norm kernel are
+// resident per SM at its register count, so the grid is one wave on GB300.
+// A constant, not derived from the device, so that results depend on n only.
+constexpr int kNormBlocksMax = 608;
 
 // Number of blocks of the norm reduction for n elements: a function of n
 // only, so the reduction order (and hence every bit of the result) is too.
@@ -61,8 +64,9 @@ struct KernelCaps {
     int step_vec, step_scalar, pack_vec, pack_scalar;
 };
 
-// Kernel launchers (kernels.cu).  All return cudaError_t as int.
-int query_kernel_caps(int sm_count, KernelCaps* caps);
+// Kernel launchers (norm.cu, step.cu, pack.cu).  All return cudaError_t as int.
+int query_step_caps(int sm_count, KernelCaps* caps);
+int query_pack_caps(int sm_count, KernelCaps* caps);
 int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
                 void* stream);

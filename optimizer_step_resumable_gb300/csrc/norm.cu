@@ -1,0 +1,182 @@
+// norm.cu -- global L2 norm of the flattened gradient and the clip factor
+// (rows a1 and a2 of the step), for sm_103a.
+//
+// "Training as a Recoverable State Transition" (aihero.club), section "The
+// Exact Targets of Clipping and AdamW": all gradients are joined into one
+// vector g; if ||g||_2 exceeds the threshold c every element is scaled by
+// c / ||g||_2.  "Grow a Language Model: Backprop" (unhomeschool.com), section
+// "Every forward op gets a backward twin", names the engine's two kernels
+// k_grad_norm_partial and k_grad_norm_final; here both levels are one
+// launch.  HBM-bound: 4 bytes per parameter.
+#include <cfloat>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace osr {
+namespace {
+
+using detail::block_sum;
+
+// (a^2 + b^2) + (c^2 + d^2): two fused multiply-adds and one add, each
+// correctly rounded in float32.
+__device__ __forceinline__ float sumsq4(float4 a)
+{
+    return __fadd_rn(__fmaf_rn(a.x, a.x, __fmul_rn(a.y, a.y)),
+                     __fmaf_rn(a.z, a.z, __fmul_rn(a.w, a.w)));
+}
+
+// Sum of squares of one run of 4*U values.  Fast path: float32 squares,
+// pairwise tree (depth 2 + log2 U), so the relative error is at most about
+// (3 + log2 U) units of 2^-24 -- 3.6e-7 for U = 8 -- and the run is flushed
+// into the caller's double accumulator.  Runs whose float32 sum leaves
+// [2^-100, FLT_MAX] (overflow, inf, nan, or values so small that squares
+// underflow) are recomputed exactly in double; all-zero runs (common for
+// embedding rows no token touched) skip that and contribute 0.
+template <int U>
+__device__ __forceinline__ double run_sumsq(const float4 (&x)[U])
+{
+    float q[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+        q[j] = sumsq4(x[j]);
+#pragma unroll
+    for (int s = 1; s < U; s <<= 1)
+#pragma unroll
+        for (int j = 0; j + s < U; j += 2 * s)
+            q[j] = __fadd_rn(q[j], q[j + s]);
+    const float r = q[0];
+    if (r >= 0x1p-100f && r <= FLT_MAX)
+        return double(r);
+    unsigned bits = 0;
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+        bits |= (__float_as_uint(x[j].x) | __float_as_uint(x[j].y) |
+                 __float_as_uint(x[j].z) | __float_as_uint(x[j].w)) & 0x7fffffffu;
+    if (bits == 0)
+        return 0.0;
+    double d = 0.0;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        d += double(x[j].x) * double(x[j].x);
+        d += double(x[j].y) * double(x[j].y);
+        d += double(x[j].z) * double(x[j].z);
+        d += double(x[j].w) * double(x[j].w);
+    }
+    return d;
+}
+
+// ---------------------------------------------------------------------------
+// Global L2 norm, two levels in one launch.
+//
+// Level 1: the flat vector is cut into tiles of kNormTileElems elements;
+// block b takes tiles b, b + P, b + 2P, ... (P = norm_blocks(n), a function
+// of n alone).  Thread t of a tile holds U = kNormVecPerThread float4s at
+// float4 index j*256 + t (coalesced), sums their squares as one run, and
+// adds the run into a double.  The block's doubles are summed with a fixed
+// shuffle tree into partials[b].
+// Level 2: the block that finishes last (atomic ticket) sums partials[0..P)
+// in a fixed order -- independent of which block that is -- takes the square
+// root and the clip factor, and publishes the result.  No block waits on
+// another; the ticket counter is reset for the next launch.
+// ---------------------------------------------------------------------------
+template <bool kVec>
+__global__ void __launch_bounds__(kNormThreads)
+    k_grad_norm(const float* __restrict__ g, int64_t n, double clip,
+                double* __restrict__ partials, unsigned int* __restrict__ counter,
+                NormResult* __restrict__ d_res, NormResult* h_res)
+{
+    constexpr int U = kNormVecPerThread;
+    const int tid = threadIdx.x;
+    const int64_t ntiles = (n + kNormTileElems - 1) / kNormTileElems;
+    const int64_t nfull = n / kNormTileElems;
+    double acc = 0.0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t base = tile * kNormTileElems;
+        float4 x[U];
+        if (tile < nfull) {
+            if (kVec) {
+                const float4* p = reinterpret_cast<const float4*>(g + base) + tid;
+#pragma unroll
+                for (int j = 0; j < U; ++j)
+                    x[j] = __ldcs(p + j * kNormThreads);
+            } else {
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const float* p = g + base + (int64_t(j * kNormThreads + tid) << 2);
+                    x[j] = make_float4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t e = base + (int64_t(j * kNormThreads + tid) << 2);
+                x[j].x = e < n ? g[e] : 0.0f;
+                x[j].y = e + 1 < n ? g[e + 1] : 0.0f;
+                x[j].z = e + 2 < n ? g[e + 2] : 0.0f;
+                x[j].w = e + 3 < n ? g[e + 3] : 0.0f;
+            }
+        }
+        acc += run_sumsq<U>(x);
+    }
+
+    acc = block_sum<kNormThreads>(acc);
+    __shared__ bool is_last;
+    if (tid == 0) {
+        partials[blockIdx.x] = acc;
+        __threadfence();
+        const unsigned ticket = atomicAdd(counter, 1u);
+        is_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!is_last)
+        return;
+    __threadfence();
+    double s = 0.0;
+    for (int i = tid; i < int(gridDim.x); i += kNormThreads)
+        s += __ldcg(partials + i);
+    s = block_sum<kNormThreads>(s);
+    if (tid == 0) {
+        NormResult r;
+        r.sumsq = s;
+        r.norm = sqrt(s);
+        const bool finite = isfinite(r.norm);
+        r.nonfinite = finite ? 0 : 1;
+        r.scale = (finite && r.norm > clip) ? float(clip / r.norm) : 1.0f;
+        r.seq = d_res->seq + 1u;
+        r.pad = 0;
+        *d_res = r;
+        if (h_res) {
+            volatile NormResult* h = h_res;
+            h->sumsq = r.sumsq;
+            h->norm = r.norm;
+            h->scale = r.scale;
+            h->nonfinite = r.nonfinite;
+            h->seq = r.seq;
+            __threadfence_system();
+        }
+        *counter = 0u;
+    }
+}
+
+}  // namespace
+
+int launch_norm(const float* g, int64_t n, double clip, double* partials,
+                unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                void* stream)
+{
+    const int blocks = norm_blocks(n);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (detail::aligned16(g))
+        k_grad_norm<true><<<blocks, kNormThreads, 0, s>>>(g, n, clip, partials, counter,
+                                                           d_res, h_res_dev);
+    else
+        k_grad_norm<false><<<blocks, kNormThreads, 0, s>>>(g, n, clip, partials, counter,
+                                                            d_res, h_res_dev);
+    return int(cudaGetLastError());
+}
+
+}  // namespace osr

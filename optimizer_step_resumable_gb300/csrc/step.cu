@@ -1,0 +1,160 @@
+// step.cu -- the fused clip-scale + AdamW pass (rows a3 and a4 of the step),
+// for sm_103a.
+//
+// "Training as a Recoverable State Transition" (aihero.club), section "The
+// Exact Targets of Clipping and AdamW": m = beta1 m + (1 - beta1) g,
+// v = beta2 v + (1 - beta2) g^2, bias corrections 1 - beta^t, and the
+// decoupled decay w (1 - lr wd) applied before subtracting
+// lr m_hat / (sqrt(v_hat) + eps), for every parameter.  The clip factor is
+// applied here to each gradient element as it is read, so the gradient is
+// never rescaled in memory (the engine's k_grad_scale pass of "Grow a
+// Language Model: Backprop" is folded in).  HBM-bound: 28 bytes per
+// parameter (read w, g, m, v; write w, m, v).
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace osr {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Fused clip + AdamW: one element.  Every operation is an explicitly
+// rounded float32 intrinsic (IEEE square root and division; no fast-math),
+// in this order:
+//   g_hat = g s
+//   m     = beta1 m + (1 - beta1) g_hat             (one fma)
+//   v     = beta2 v + ((1 - beta2) g_hat) g_hat      (one fma; the factor
+//                                                     first, so g_hat^2 never
+//                                                     overflows on its own)
+//   denom = sqrt(v) / sqrt(1 - beta2^t) + eps        (one fma) = sqrt(v_hat)+eps
+//   w     = w (1 - lr wd) - (lr / (1 - beta1^t)) (m / denom)      (one fma)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void adamw_elem(float& w, float g, float& m, float& v,
+                                           float s, const StepScalars& k)
+{
+    const float gh = __fmul_rn(g, s);
+    m = __fmaf_rn(k.beta1, m, __fmul_rn(k.omb1, gh));
+    v = __fmaf_rn(k.beta2, v, __fmul_rn(__fmul_rn(k.omb2, gh), gh));
+    const float denom = __fmaf_rn(__fsqrt_rn(v), k.inv_sqrt_bc2, k.eps);
+    const float upd = __fmul_rn(k.step_size, __fdiv_rn(m, denom));
+    w = __fmaf_rn(w, k.decay, -upd);
+}
+
+__device__ __forceinline__ void adamw4(float4& w, float4 g, float4& m, float4& v,
+                                       float s, const StepScalars& k)
+{
+    adamw_elem(w.x, g.x, m.x, v.x, s, k);
+    adamw_elem(w.y, g.y, m.y, v.y, s, k);
+    adamw_elem(w.z, g.z, m.z, v.z, s, k);
+    adamw_elem(w.w, g.w, m.w, v.w, s, k);
+}
+
+constexpr int kStepThreads = 256;
+constexpr int kStepVec = 2;  // float4 of each array per thread per chunk
+
+// Reads w, g, m, v once and writes w, m, v once (28 bytes per parameter).
+// The clip factor and the non-finite flag come from the norm kernel's
+// result in device memory, so nothing returns to the host between kernels.
+template <bool kVec>
+__global__ void __launch_bounds__(kStepThreads)
+    k_clip_adamw(float* __restrict__ w, const float* __restrict__ g,
+                 float* __restrict__ m, float* __restrict__ v, int64_t n,
+                 StepScalars k, const NormResult* __restrict__ res)
+{
+    if (res->nonfinite)
+        return;
+    const float s = res->scale;
+    const int64_t gtid = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
+    const int64_t stride = int64_t(gridDim.x) * kStepThreads;
+    if (kVec) {
+        float4* w4 = reinterpret_cast<float4*>(w);
+        const float4* g4 = reinterpret_cast<const float4*>(g);
+        float4* m4 = reinterpret_cast<float4*>(m);
+        float4* v4 = reinterpret_cast<float4*>(v);
+        const int64_t n4 = n >> 2;
+        constexpr int64_t chunk = int64_t(kStepThreads) * kStepVec;
+        const int64_t nchunks = n4 / chunk;
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            const int64_t i0 = c * chunk + threadIdx.x;
+            float4 W[kStepVec], G[kStepVec], M[kStepVec], V[kStepVec];
+#pragma unroll
+            for (int j = 0; j < kStepVec; ++j) {
+                const int64_t i = i0 + j * kStepThreads;
+                W[j] = __ldcs(w4 + i);
+                G[j] = __ldcs(g4 + i);
+                M[j] = __ldcs(m4 + i);
+                V[j] = __ldcs(v4 + i);
+            }
+#pragma unroll
+            for (int j = 0; j < kStepVec; ++j)
+                adamw4(W[j], G[j], M[j], V[j], s, k);
+#pragma unroll
+            for (int j = 0; j < kStepVec; ++j) {
+                const int64_t i = i0 + j * kStepThreads;
+                __stcs(w4 + i, W[j]);
+                __stcs(m4 + i, M[j]);
+                __stcs(v4 + i, V[j]);
+            }
+        }
+        for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
+            float4 W = __ldcs(w4 + i), G = __ldcs(g4 + i), M = __ldcs(m4 + i),
+                   V = __ldcs(v4 + i);
+            adamw4(W, G, M, V, s, k);
+            __stcs(w4 + i, W);
+            __stcs(m4 + i, M);
+            __stcs(v4 + i, V);
+        }
+        if (gtid < (n & 3)) {
+            const int64_t e = (n4 << 2) + gtid;
+            float W = w[e], M = m[e], V = v[e];
+            adamw_elem(W, g[e], M, V, s, k);
+            w[e] = W;
+            m[e] = M;
+            v[e] = V;
+        }
+    } else {
+        for (int64_t e = gtid; e < n; e += stride) {
+            float W = __ldcs(w + e), M = __ldcs(m + e), V = __ldcs(v + e);
+            adamw_elem(W, __ldcs(g + e), M, V, s, k);
+            __stcs(w + e, W);
+            __stcs(m + e, M);
+            __stcs(v + e, V);
+        }
+    }
+}
+
+}  // namespace
+
+int query_step_caps(int sm_count, KernelCaps* caps)
+{
+    caps->step_vec = detail::resident_blocks(reinterpret_cast<const void*>(&k_clip_adamw<true>),
+                                             kStepThreads, sm_count);
+    caps->step_scalar = detail::resident_blocks(
+        reinterpret_cast<const void*>(&k_clip_adamw<false>), kStepThreads, sm_count);
+    return int(cudaGetLastError());
+}
+
+int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
+                 const StepScalars& k, const NormResult* d_res, const KernelCaps& caps,
+                 void* stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool vec = detail::aligned16(w) && detail::aligned16(g) && detail::aligned16(m) && detail::aligned16(v);
+    if (vec) {
+        const int cap = caps.step_vec;
+        const int64_t want = detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec);
+        const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
+        k_clip_adamw<true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+    } else {
+        const int cap = caps.step_scalar;
+        const int64_t want = detail::ceil_div(n, kStepThreads);
+        const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
+        k_clip_adamw<false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+    }
+    return int(cudaGetLastError());
+}
+
+}  // namespace osr
