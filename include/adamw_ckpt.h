@@ -192,6 +192,39 @@ ADAMW_API int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out,
               float* d_w, float* d_m, float* d_v, void* stream);
 
 /*
+ * One clipped-AdamW step with no context and no allocation, for callers that
+ * must not allocate GPU memory: code running under a framework or server that
+ * owns all device memory through its own pool, plug-ins handed nothing but
+ * their input and output buffers, and latency-critical paths where
+ * cudaMalloc / cudaFree would synchronise the device.  The pages have no
+ * counterpart: this is a packaging of the same two kernels as
+ * adamw_clip_step.
+ *
+ * Same arguments and arithmetic as adamw_clip_step (n parameters, flat
+ * layout, 1-based t, beta1/beta2/eps given per call), same results bit for
+ * bit.  If d_norm_out is not NULL, the gradient norm (double) is written to
+ * that device address on `stream`; a non-finite norm leaves w, m, v
+ * untouched and shows there as inf/nan (the call does not wait, so it cannot
+ * return ADAMW_ENONFINITE).
+ *
+ * Scratch: a 5,120-byte array in the library's static device memory, which
+ * every GPU that loads the library keeps until the process exits; it serves
+ * any n in [1, 2^31 - 1] (the reduction grid is capped); n outside that range
+ * is rejected with ADAMW_EINVAL.  The first call on each device resolves
+ * that array's address and the kernels' launch limits (no allocation); make
+ * that first call before any stream capture.  All calls share the one array
+ * and it keeps the last call's contents (each call clears the part that must
+ * start at zero): calls that overlap on the GPU -- on different streams or
+ * from different threads without ordering -- race and give wrong results.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+ADAMW_API int adamw_clip_step_noalloc(float* d_w, const float* d_g, float* d_m,
+                                      float* d_v, int64_t n, int32_t t,
+                                      double lr, double wd, double clip,
+                                      double beta1, double beta2, double eps,
+                                      double* d_norm_out, void* stream);
+
+/*
  * Host-only helpers (no GPU needed).
  *
  * ckpt_file_size: 8 + 12 n ([C] "Total size"); -1 if n is outside

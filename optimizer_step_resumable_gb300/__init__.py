@@ -36,6 +36,9 @@ SIGNATURES = {
                                    _c.c_double, _c.c_double, _vp]),
     "adamw_last_norm": (_c.c_int, [_vp, _c.POINTER(_c.c_double), _c.POINTER(_c.c_float)]),
     "adamw_record_events": (_c.c_int, [_vp, _vp, _vp, _vp]),
+    "adamw_clip_step_noalloc": (_c.c_int, [_vp, _vp, _vp, _vp, _c.c_int64, _c.c_int32,
+                                           _c.c_double, _c.c_double, _c.c_double,
+                                           _c.c_double, _c.c_double, _c.c_double, _vp, _vp]),
     "ckpt_pack": (_c.c_int, [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "ckpt_write": (_c.c_int, [_vp, _c.c_char_p, _c.c_char_p, _c.c_size_t]),
     "ckpt_read": (_c.c_int, [_vp, _c.c_char_p, _c.POINTER(_c.c_int32), _vp, _vp, _vp, _vp]),
@@ -197,6 +200,26 @@ def adamw_last_norm(ctx: Context):
     st = library().adamw_last_norm(ctx.handle, ctypes.byref(norm), ctypes.byref(scale))
     _check(st, "adamw_last_norm")
     return norm.value, scale.value
+
+
+def adamw_clip_step_noalloc(w, g, m, v, t: int, lr: float, wd: float, clip: float,
+                            beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                            norm_out=None, stream=None):
+    """The clipped-AdamW step without a context, for callers that must not
+    allocate GPU memory (see include/adamw_ckpt.h).  norm_out: optional
+    float64 CUDA tensor of one element that receives the gradient norm."""
+    import torch
+    n = w.numel()
+    np_ = None
+    if norm_out is not None:
+        if not (norm_out.is_cuda and norm_out.dtype == torch.float64 and norm_out.numel() >= 1):
+            raise TypeError("norm_out must be a float64 CUDA tensor")
+        np_ = norm_out.data_ptr()
+    st = library().adamw_clip_step_noalloc(
+        _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"), _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"),
+        int(n), int(t), float(lr), float(wd), float(clip), float(beta1), float(beta2),
+        float(eps), np_, _stream(stream))
+    _check(st, "adamw_clip_step_noalloc")
 
 
 def adamw_record_events(ctx: Context, ev_begin=None, ev_mid=None, ev_end=None):

@@ -24,7 +24,7 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler",
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
              "-I" + INCLUDE]
 
-CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu"]
+CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu", "noalloc.cu"]
 CXX_SOURCES = ["ckpt_io.cpp"]
 
 
