@@ -66,6 +66,18 @@ extern "C" {
 /* adamw_create flags. */
 #define ADAMW_CREATE_NO_CKPT 1 /* do not allocate the checkpoint staging    */
 
+/* ckpt_set_options / ckpt_write_image flags. */
+#define CKPT_DIRECT 1 /* write with O_DIRECT when the file system allows it */
+
+/* Checkpoint requests recorded by the signal handlers (ckpt_signals_*). */
+#define CKPT_REQ_WRITE 1 /* SIGUSR1: write a checkpoint, keep training     */
+#define CKPT_REQ_EXIT 2  /* SIGTERM: write a checkpoint, then stop         */
+
+/* ckpt_step_end actions. */
+#define CKPT_ACTION_NONE 0    /* no checkpoint at this step                 */
+#define CKPT_ACTION_WRITING 1 /* packed; being written in the background    */
+#define CKPT_ACTION_EXIT 2    /* written and durable; the caller should exit */
+
 typedef struct adamw_ctx adamw_ctx;
 
 /*
@@ -168,16 +180,65 @@ ADAMW_API int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w,
               void* side_stream);
 
 /*
- * Checkpoint, part 2 ([S] "Atomic write"): waits for the copy started by
- * the last ckpt_pack, writes the image to <dir>/step_%06d.bin.tmp, fsyncs
- * it, renames it to <dir>/step_%06d.bin and fsyncs dir.  A crash before the
- * rename leaves any previous file of that name intact.  The final path is
- * copied to path_out (may be NULL) if it fits in path_cap bytes.
- * ADAMW_ESTATE if there is no packed image; ADAMW_EIO on any file error
- * (the .tmp file is removed).  Blocks the calling host thread.
+ * Checkpoint, part 2 ([S] "Atomic write"): waits for the copy started by the
+ * last ckpt_pack, writes the image to <dir>/step_%06d.bin.tmp, fsyncs it,
+ * renames it to <dir>/step_%06d.bin and fsyncs dir.  A crash before the
+ * rename leaves any previous file of that name intact.  With CKPT_DIRECT
+ * (the default; see ckpt_set_options) the pinned image goes to the disk with
+ * O_DIRECT where the file system allows it, else through the page cache.
+ * After the rename, rotation (if set) deletes all but the newest `keep`
+ * step_*.bin files of dir.  The final path is copied to path_out (may be
+ * NULL) if it fits in path_cap bytes.  ADAMW_ESTATE if there is no packed
+ * image; ADAMW_EIO on any file error (the .tmp file is removed).
+ *
+ * ckpt_write blocks the calling thread until the file is durable.
+ * ckpt_write_async hands the same work to the context's writer thread and
+ * returns at once ([S] "Production patterns": asynchronous writes so that
+ * training continues); ckpt_wait blocks until that write is done and returns
+ * its status and path (ADAMW_OK and "" if none was started).  One write is in
+ * flight at most: ckpt_write_async, ckpt_pack, ckpt_read and
+ * ckpt_set_options first wait (on the host) for a write in flight.  A failed
+ * asynchronous write not yet reported by ckpt_wait is reported by the next
+ * ckpt_write_async.
  */
 ADAMW_API int ckpt_write(adamw_ctx* ctx, const char* dir, char* path_out,
-               size_t path_cap);
+                         size_t path_cap);
+ADAMW_API int ckpt_write_async(adamw_ctx* ctx, const char* dir);
+ADAMW_API int ckpt_wait(adamw_ctx* ctx, char* path_out, size_t path_cap);
+
+/*
+ * Writer options: keep >= 1 keeps only the newest `keep` step_*.bin files of
+ * the target directory after each write ([S] "Production patterns": rotation
+ * keeps the last K checkpoints so the disk does not fill); keep = 0 keeps
+ * all.  flags: CKPT_DIRECT or 0.  Defaults: keep = 0, CKPT_DIRECT.
+ */
+ADAMW_API int ckpt_set_options(adamw_ctx* ctx, int32_t keep, int32_t flags);
+
+/*
+ * Checkpoint policy at a step boundary ([C] "Five decisions": every 100
+ * steps; "SIGTERM & SIGUSR1": finish the step, then write; SIGTERM then
+ * exits, SIGUSR1 continues).  Call after the optimizer step of `step`
+ * (completed updates) has been launched.  Writes when step > 0 and
+ * step % every == 0 (every = 0: only on signals) or when a signal recorded
+ * by ckpt_signals_install is pending (the request is consumed).  On a
+ * SIGTERM request the write completes before the call returns and
+ * *action_out = CKPT_ACTION_EXIT: the caller should stop training; otherwise
+ * the write runs in the background (CKPT_ACTION_WRITING) or nothing happens
+ * (CKPT_ACTION_NONE).  The library never exits the process itself.
+ */
+ADAMW_API int ckpt_step_end(adamw_ctx* ctx, int32_t step, const float* d_w,
+                            const float* d_m, const float* d_v, void* main_stream,
+                            void* side_stream, const char* dir, int32_t every,
+                            int32_t* action_out);
+
+/*
+ * Installs handlers that record SIGUSR1 (mask bit CKPT_REQ_WRITE) and
+ * SIGTERM (CKPT_REQ_EXIT) as checkpoint requests instead of their default
+ * actions; the handlers only set a lock-free flag.  ckpt_signals_take
+ * returns the pending request bits and clears them (async-signal-safe).
+ */
+ADAMW_API int ckpt_signals_install(int32_t mask);
+ADAMW_API int32_t ckpt_signals_take(void);
 
 /*
  * Resume ([C] "Why save m & v"; [S] "Three failure modes"): opens path,
@@ -236,6 +297,16 @@ ADAMW_API int adamw_clip_step_noalloc(float* d_w, const float* d_g, float* d_m,
  * ckpt_probe: validates a file the way ckpt_read does (header, sign, size)
  * without reading the arrays; *step_out and *n_out (may be NULL) receive the
  * header fields.  n_expected < 0 skips the n comparison.
+ *
+ * ckpt_write_image: the atomic writer applied to a complete host image of
+ * `bytes` bytes (header included; the header must describe exactly that
+ * size).  With CKPT_DIRECT, an image at a 4096-byte aligned address with
+ * capacity >= bytes rounded up to 4096 is written with O_DIRECT when the
+ * file system allows it (the padding past `bytes` is written, then cut off).
+ *
+ * ckpt_rotate: deletes all but the newest `keep` files named
+ * step_<digits>.bin in dir (keep = 0: none); *removed (may be NULL) receives
+ * the count.
  */
 ADAMW_API int64_t ckpt_file_size(int64_t n);
 ADAMW_API int ckpt_write_host(const char* dir, int32_t step, int32_t n,
@@ -243,6 +314,10 @@ ADAMW_API int ckpt_write_host(const char* dir, int32_t step, int32_t n,
                     char* path_out, size_t path_cap);
 ADAMW_API int ckpt_probe(const char* path, int32_t n_expected, int32_t* step_out,
                int32_t* n_out);
+ADAMW_API int ckpt_write_image(const char* dir, const void* image, int64_t bytes,
+                               int64_t capacity, int32_t flags, char* path_out,
+                               size_t path_cap);
+ADAMW_API int ckpt_rotate(const char* dir, int32_t keep, int32_t* removed);
 
 /* Name of a status code, and the last failure's explanation (this thread). */
 ADAMW_API const char* adamw_strerror(int status);

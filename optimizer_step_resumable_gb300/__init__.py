@@ -20,6 +20,9 @@ LIBRARY = os.path.join(PKG, "liboptstep.so")
 OK = 0
 EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9, -1)
 CREATE_NO_CKPT = 1
+CKPT_DIRECT = 1
+CKPT_REQ_WRITE, CKPT_REQ_EXIT = 1, 2
+CKPT_ACTION_NONE, CKPT_ACTION_WRITING, CKPT_ACTION_EXIT = 0, 1, 2
 
 # ABI: name -> (restype, argtypes)
 _c = ctypes
@@ -41,6 +44,16 @@ SIGNATURES = {
                                            _c.c_double, _c.c_double, _c.c_double, _vp, _vp]),
     "ckpt_pack": (_c.c_int, [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp]),
     "ckpt_write": (_c.c_int, [_vp, _c.c_char_p, _c.c_char_p, _c.c_size_t]),
+    "ckpt_write_async": (_c.c_int, [_vp, _c.c_char_p]),
+    "ckpt_wait": (_c.c_int, [_vp, _c.c_char_p, _c.c_size_t]),
+    "ckpt_set_options": (_c.c_int, [_vp, _c.c_int32, _c.c_int32]),
+    "ckpt_step_end": (_c.c_int, [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_char_p,
+                                 _c.c_int32, _c.POINTER(_c.c_int32)]),
+    "ckpt_signals_install": (_c.c_int, [_c.c_int32]),
+    "ckpt_signals_take": (_c.c_int32, []),
+    "ckpt_write_image": (_c.c_int, [_c.c_char_p, _vp, _c.c_int64, _c.c_int64, _c.c_int32,
+                                    _c.c_char_p, _c.c_size_t]),
+    "ckpt_rotate": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.POINTER(_c.c_int32)]),
     "ckpt_read": (_c.c_int, [_vp, _c.c_char_p, _c.POINTER(_c.c_int32), _vp, _vp, _vp, _vp]),
     "ckpt_file_size": (_c.c_int64, [_c.c_int64]),
     "ckpt_write_host": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_int32, _vp, _vp, _vp,
@@ -243,6 +256,64 @@ def ckpt_write(ctx: Context, directory: str) -> str:
     st = library().ckpt_write(ctx.handle, os.fsencode(directory), buf, len(buf))
     _check(st, "ckpt_write")
     return buf.value.decode()
+
+
+def ckpt_write_async(ctx: Context, directory: str):
+    _check(library().ckpt_write_async(ctx.handle, os.fsencode(directory)), "ckpt_write_async")
+
+
+def ckpt_wait(ctx: Context) -> str:
+    """Path of the last asynchronous write ('' if none); raises on failure."""
+    buf = ctypes.create_string_buffer(4200)
+    _check(library().ckpt_wait(ctx.handle, buf, len(buf)), "ckpt_wait")
+    return buf.value.decode()
+
+
+def ckpt_set_options(ctx: Context, keep: int = 0, flags: int = CKPT_DIRECT):
+    _check(library().ckpt_set_options(ctx.handle, int(keep), int(flags)), "ckpt_set_options")
+
+
+def ckpt_step_end(ctx: Context, step: int, w, m, v, directory: str, every: int,
+                  main_stream=None, side_stream=None) -> int:
+    """Checkpoint policy at a step boundary; returns a CKPT_ACTION_* value."""
+    n = ctx.n
+    ms = _stream(main_stream)
+    ss = ms if side_stream is None else _stream(side_stream)
+    action = ctypes.c_int32(0)
+    st = library().ckpt_step_end(ctx.handle, int(step), _dev_ptr(w, n, "w"),
+                                 _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), ms, ss,
+                                 os.fsencode(directory), int(every), ctypes.byref(action))
+    _check(st, "ckpt_step_end")
+    return action.value
+
+
+def ckpt_signals_install(mask: int = CKPT_REQ_WRITE | CKPT_REQ_EXIT):
+    _check(library().ckpt_signals_install(int(mask)), "ckpt_signals_install")
+
+
+def ckpt_signals_take() -> int:
+    return library().ckpt_signals_take()
+
+
+def ckpt_write_image(directory: str, image, bytes_: int = None, flags: int = CKPT_DIRECT) -> str:
+    """Atomic write of a complete host image (numpy uint8 array, header
+    included); the array may be longer than the file (padding for O_DIRECT)."""
+    import numpy as np
+    if not (isinstance(image, np.ndarray) and image.dtype == np.uint8 and image.flags.c_contiguous):
+        raise TypeError("image must be a contiguous uint8 numpy array")
+    nbytes = image.size if bytes_ is None else int(bytes_)
+    buf = ctypes.create_string_buffer(4200)
+    st = library().ckpt_write_image(os.fsencode(directory), image.ctypes.data, nbytes,
+                                    image.size, int(flags), buf, len(buf))
+    _check(st, "ckpt_write_image")
+    return buf.value.decode()
+
+
+def ckpt_rotate(directory: str, keep: int) -> int:
+    removed = ctypes.c_int32(0)
+    _check(library().ckpt_rotate(os.fsencode(directory), int(keep), ctypes.byref(removed)),
+           "ckpt_rotate")
+    return removed.value
 
 
 def ckpt_read(ctx: Context, path: str, w, m, v, stream=None) -> int:

@@ -24,7 +24,7 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler",
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
              "-I" + INCLUDE]
 
-CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu", "noalloc.cu"]
+CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu", "writer.cu", "noalloc.cu"]
 CXX_SOURCES = ["ckpt_io.cpp"]
 
 
@@ -36,7 +36,7 @@ def nvcc() -> str:
 
 def _sources():
     return ([os.path.join(CSRC, s) for s in CUDA_SOURCES + CXX_SOURCES]
-            + [os.path.join(CSRC, h) for h in ("internal.h", "common.cuh")]
+            + [os.path.join(CSRC, h) for h in ("internal.h", "common.cuh", "context.h")]
             + [os.path.join(INCLUDE, "adamw_ckpt.h")])
 
 

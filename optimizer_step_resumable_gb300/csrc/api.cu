@@ -10,40 +10,8 @@
 #include <cuda_runtime.h>
 #include <unistd.h>
 
+#include "context.h"
 #include "internal.h"
-
-struct adamw_ctx {
-    int64_t n = 0;
-    std::vector<int64_t> offsets, numels;
-    int device = -1;
-    int sm_count = 0;
-    osr::KernelCaps caps{};
-    double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
-
-    // norm scratch: [NormResult | counter | pad][partials x kNormBlocksMax]
-    unsigned char* d_scratch = nullptr;
-    osr::NormResult* d_res = nullptr;
-    unsigned int* d_counter = nullptr;
-    double* d_partials = nullptr;
-    osr::NormResult* h_res = nullptr;      // pinned, mapped: host view
-    osr::NormResult* h_res_dev = nullptr;  // device view of the same memory
-    cudaEvent_t ev_norm = nullptr;
-    bool norm_launched = false;
-    cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
-
-    // checkpoint staging: image = alloc + 8, so the w region (image + 8)
-    // starts on a 16-byte boundary
-    bool has_ckpt = false;
-    unsigned char* d_image_alloc = nullptr;
-    unsigned char* h_image_alloc = nullptr;
-    cudaEvent_t ev_pack = nullptr, ev_d2h = nullptr;
-    bool packed = false, d2h_pending = false;
-    int32_t packed_step = -1;
-
-    unsigned char* d_image() const { return d_image_alloc + 8; }
-    unsigned char* h_image() const { return h_image_alloc + 8; }
-    size_t image_bytes() const { return size_t(8 + 12 * n); }
-};
 
 namespace {
 
@@ -99,6 +67,7 @@ void free_ctx(adamw_ctx* c)
 {
     if (!c)
         return;
+    osr::writer_stop(c);
     if (c->device >= 0) {
         DeviceScope scope(c->device);
         if (c->ev_d2h && c->d2h_pending)
@@ -248,8 +217,8 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
             c->d_image_alloc = nullptr;
             return bail(cuda_fail(e, "cudaMalloc(checkpoint staging)"));
         }
-        if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_image_alloc), bytes,
-                               cudaHostAllocDefault)) != cudaSuccess) {
+        if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_image_alloc),
+                               c->h_image_capacity(), cudaHostAllocDefault)) != cudaSuccess) {
             c->h_image_alloc = nullptr;
             return bail(cuda_fail(e, "cudaHostAlloc(checkpoint image)"));
         }
@@ -391,6 +360,8 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
         return rc;
     if (step < 0)
         return fail(ADAMW_EINVAL, "step=%d is negative", step);
+    // The pinned image may still be read by a write in flight.
+    osr::writer_drain(ctx);
     DeviceScope scope(ctx->device);
     cudaStream_t mainst = static_cast<cudaStream_t>(main_stream);
     cudaStream_t side = static_cast<cudaStream_t>(side_stream);
@@ -413,22 +384,6 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
     return ADAMW_OK;
 }
 
-int ckpt_write(adamw_ctx* ctx, const char* dir, char* path_out, size_t path_cap)
-{
-    osr::clear_error();
-    if (!ctx || !dir)
-        return fail(ADAMW_EINVAL, "ctx or dir is NULL");
-    if (!ctx->packed)
-        return fail(ADAMW_ESTATE, "no packed checkpoint: call ckpt_pack first");
-    {
-        DeviceScope scope(ctx->device);
-        CUDA_TRY(cudaEventSynchronize(ctx->ev_d2h));
-    }
-    ctx->d2h_pending = false;
-    const osr::IoPiece piece{ctx->h_image(), ctx->image_bytes()};
-    return osr::write_file_atomic(dir, ctx->packed_step, &piece, 1, path_out, path_cap);
-}
-
 int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out, float* d_w, float* d_m,
               float* d_v, void* stream)
 {
@@ -441,6 +396,7 @@ int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out, float* d_w, f
     if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_m, "d_m")) ||
         (rc = check_state_ptr(d_v, "d_v")))
         return rc;
+    osr::writer_drain(ctx);
     DeviceScope scope(ctx->device);
     if (ctx->d2h_pending) {
         CUDA_TRY(cudaEventSynchronize(ctx->ev_d2h));

@@ -15,9 +15,16 @@
 #include <cstdio>
 #include <cstring>
 
+#include <algorithm>
+#include <atomic>
+#include <csignal>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include <dirent.h>
 #include <fcntl.h>
 #include <sys/stat.h>
-#include <sys/uio.h>
 #include <unistd.h>
 
 #include "internal.h"
@@ -41,13 +48,17 @@ void put_le32(unsigned char* p, uint32_t x)
         p[i] = static_cast<unsigned char>((x >> (8 * i)) & 0xffu);
 }
 
+}  // namespace
+
 uint32_t get_le32(const unsigned char* p)
 {
     return uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16) |
            (uint32_t(p[3]) << 24);
 }
 
-int write_exact(int fd, const void* src, size_t bytes, const char* path)
+namespace {
+
+int write_exact(int fd, const void* src, size_t bytes, const char* path, int* err_out = nullptr)
 {
     const unsigned char* p = static_cast<const unsigned char*>(src);
     while (bytes > 0) {
@@ -55,9 +66,12 @@ int write_exact(int fd, const void* src, size_t bytes, const char* path)
         const size_t want = bytes > (size_t(1) << 30) ? (size_t(1) << 30) : bytes;
         const ssize_t got = ::write(fd, p, want);
         if (got < 0) {
-            if (errno == EINTR)
+            const int e = errno;
+            if (e == EINTR)
                 continue;
-            return fail(ADAMW_EIO, "write %s: %s", path, std::strerror(errno));
+            if (err_out)
+                *err_out = e;
+            return fail(ADAMW_EIO, "write %s: %s", path, std::strerror(e));
         }
         p += got;
         bytes -= size_t(got);
@@ -99,7 +113,7 @@ int read_exact(int fd, void* dst, size_t bytes, const char* path)
 }
 
 int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
-                      int npieces, char* path_out, size_t path_cap)
+                      int npieces, char* path_out, size_t path_cap, int32_t flags)
 {
     if (!dir || step < 0)
         return fail(ADAMW_EINVAL, "ckpt write: null directory or negative step");
@@ -112,12 +126,43 @@ int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
         return fail(ADAMW_EINVAL, "ckpt write: directory name too long");
     std::snprintf(tmp_path, sizeof tmp_path, "%s.tmp", final_path);
 
-    const int fd = ::open(tmp_path, O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC, 0644);
+    // O_DIRECT moves the pinned image straight to the device (no page-cache
+    // copy); it needs a block-aligned buffer, length and offset, so the last
+    // partial block is written whole from the buffer's padding and the file
+    // is then truncated to its exact size.
+    const bool want_direct = (flags & kWriteDirect) && npieces == 1 &&
+                             (reinterpret_cast<uintptr_t>(pieces[0].data) % kIoBlock) == 0 &&
+                             pieces[0].capacity >= round_up_block(pieces[0].bytes);
+    int fd = -1;
+    bool direct = false;
+    if (want_direct) {
+        fd = ::open(tmp_path, O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC | O_DIRECT, 0644);
+        direct = fd >= 0;
+    }
+    if (fd < 0)  // not requested, or refused by the file system (e.g. EINVAL)
+        fd = ::open(tmp_path, O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC, 0644);
     if (fd < 0)
         return fail(ADAMW_EIO, "open %s: %s", tmp_path, std::strerror(errno));
     int rc = ADAMW_OK;
-    for (int i = 0; i < npieces && rc == ADAMW_OK; ++i)
-        rc = write_exact(fd, pieces[i].data, pieces[i].bytes, tmp_path);
+    if (direct) {
+        const size_t whole = round_up_block(pieces[0].bytes);
+        int werr = 0;
+        rc = write_exact(fd, pieces[0].data, whole, tmp_path, &werr);
+        if (rc != ADAMW_OK && werr == EINVAL) {
+            // the device refused this alignment after all: rewrite buffered
+            ::close(fd);
+            fd = ::open(tmp_path, O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC, 0644);
+            if (fd < 0)
+                return fail(ADAMW_EIO, "open %s: %s", tmp_path, std::strerror(errno));
+            direct = false;
+            rc = write_exact(fd, pieces[0].data, pieces[0].bytes, tmp_path);
+        } else if (rc == ADAMW_OK && ::ftruncate(fd, off_t(pieces[0].bytes)) != 0) {
+            rc = fail(ADAMW_EIO, "ftruncate %s: %s", tmp_path, std::strerror(errno));
+        }
+    } else {
+        for (int i = 0; i < npieces && rc == ADAMW_OK; ++i)
+            rc = write_exact(fd, pieces[i].data, pieces[i].bytes, tmp_path);
+    }
     if (rc == ADAMW_OK && ::fsync(fd) != 0)
         rc = fail(ADAMW_EIO, "fsync %s: %s", tmp_path, std::strerror(errno));
     if (::close(fd) != 0 && rc == ADAMW_OK)
@@ -142,6 +187,47 @@ int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
         std::memcpy(path_out, final_path, size_t(len) + 1);
     }
     return ADAMW_OK;
+}
+
+// Checkpoint rotation ("Checkpoint and Sharded Resume", lesson 80, section
+// "Production patterns in the wild": keep the last K checkpoints and delete
+// the oldest, or the disk fills up mid-run and the next write fails).
+int rotate_files(const char* dir, int32_t keep, int32_t* removed)
+{
+    if (removed)
+        *removed = 0;
+    if (!dir || keep < 0)
+        return fail(ADAMW_EINVAL, "ckpt rotate: null directory or negative keep");
+    if (keep == 0)
+        return ADAMW_OK;
+    DIR* d = ::opendir(dir);
+    if (!d)
+        return fail(ADAMW_EIO, "opendir %s: %s", dir, std::strerror(errno));
+    std::vector<std::pair<long long, std::string>> files;
+    while (struct dirent* e = ::readdir(d)) {
+        const char* nm = e->d_name;
+        const size_t L = std::strlen(nm);
+        if (L < 10 || std::strncmp(nm, "step_", 5) != 0 || std::strcmp(nm + L - 4, ".bin") != 0)
+            continue;
+        bool digits = L - 9 <= 12;
+        for (size_t i = 5; i < L - 4 && digits; ++i)
+            digits = nm[i] >= '0' && nm[i] <= '9';
+        if (!digits)
+            continue;
+        files.emplace_back(std::atoll(std::string(nm + 5, L - 9).c_str()), std::string(nm));
+    }
+    ::closedir(d);
+    std::sort(files.begin(), files.end(),
+              [](const auto& a, const auto& b) { return a.first > b.first; });
+    int rc = ADAMW_OK;
+    for (size_t i = size_t(keep); i < files.size(); ++i) {
+        const std::string p = std::string(dir) + "/" + files[i].second;
+        if (::unlink(p.c_str()) != 0)
+            rc = fail(ADAMW_EIO, "unlink %s: %s", p.c_str(), std::strerror(errno));
+        else if (removed)
+            ++*removed;
+    }
+    return rc;
 }
 
 int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
@@ -219,9 +305,69 @@ int ckpt_write_host(const char* dir, int32_t step, int32_t n, const float* h_w,
     osr::put_le32(header, uint32_t(step));
     osr::put_le32(header + 4, uint32_t(n));
     const size_t bytes = size_t(n) * 4u;
-    const osr::IoPiece pieces[4] = {{header, 8}, {h_w, bytes}, {h_m, bytes}, {h_v, bytes}};
+    const osr::IoPiece pieces[4] = {
+        {header, 8, 8}, {h_w, bytes, bytes}, {h_m, bytes, bytes}, {h_v, bytes, bytes}};
     return osr::write_file_atomic(dir, step, pieces, 4, path_out, path_cap);
 }
+
+int ckpt_write_image(const char* dir, const void* image, int64_t bytes, int64_t capacity,
+                     int32_t flags, char* path_out, size_t path_cap)
+{
+    osr::clear_error();
+    if (!image || bytes < 8 || capacity < bytes)
+        return osr::fail(ADAMW_EINVAL, "ckpt_write_image: null image or bad sizes");
+    const unsigned char* h = static_cast<const unsigned char*>(image);
+    const int32_t step = int32_t(osr::get_le32(h));
+    const int32_t n = int32_t(osr::get_le32(h + 4));
+    if (step < 0 || n < 0 || bytes != 8 + 12 * int64_t(n))
+        return osr::fail(ADAMW_EINVAL,
+                         "ckpt_write_image: header step=%d n=%d does not describe %lld bytes", step,
+                         n, (long long)bytes);
+    const osr::IoPiece piece{image, size_t(bytes), size_t(capacity)};
+    return osr::write_file_atomic(dir, step, &piece, 1, path_out, path_cap,
+                                  flags & osr::kWriteDirect);
+}
+
+int ckpt_rotate(const char* dir, int32_t keep, int32_t* removed)
+{
+    osr::clear_error();
+    return osr::rotate_files(dir, keep, removed);
+}
+
+// ---------------------------------------------------------------------------
+// Signals ("Grow a Language Model: Checkpoints", section "SIGTERM & SIGUSR1"):
+// SIGTERM = finish the step, write a checkpoint, exit; SIGUSR1 = finish the
+// step, write a checkpoint, continue.  The handler only records the request;
+// the training loop acts on it at the next step boundary.
+// ---------------------------------------------------------------------------
+namespace {
+std::atomic<int> g_signal_requests{0};
+static_assert(std::atomic<int>::is_always_lock_free, "signal flag must be lock-free");
+
+extern "C" void on_ckpt_signal(int sig)
+{
+    g_signal_requests.fetch_or(sig == SIGTERM ? CKPT_REQ_EXIT : CKPT_REQ_WRITE);
+}
+}  // namespace
+
+int ckpt_signals_install(int32_t mask)
+{
+    osr::clear_error();
+    if (mask & ~(CKPT_REQ_WRITE | CKPT_REQ_EXIT))
+        return osr::fail(ADAMW_EINVAL, "ckpt_signals_install: unknown mask bits 0x%x", mask);
+    struct sigaction sa;
+    std::memset(&sa, 0, sizeof sa);
+    sa.sa_handler = on_ckpt_signal;
+    sigemptyset(&sa.sa_mask);
+    sa.sa_flags = SA_RESTART;
+    if ((mask & CKPT_REQ_WRITE) && ::sigaction(SIGUSR1, &sa, nullptr) != 0)
+        return osr::fail(ADAMW_EINVAL, "sigaction(SIGUSR1): %s", std::strerror(errno));
+    if ((mask & CKPT_REQ_EXIT) && ::sigaction(SIGTERM, &sa, nullptr) != 0)
+        return osr::fail(ADAMW_EINVAL, "sigaction(SIGTERM): %s", std::strerror(errno));
+    return ADAMW_OK;
+}
+
+int32_t ckpt_signals_take(void) { return g_signal_requests.exchange(0); }
 
 int ckpt_probe(const char* path, int32_t n_expected, int32_t* step_out, int32_t* n_out)
 {

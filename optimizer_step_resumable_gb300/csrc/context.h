@@ -1,0 +1,85 @@
+// context.h -- the adamw_ctx object behind the C ABI (internal).
+#pragma once
+
+#include <condition_variable>
+#include <cstdint>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace osr {
+
+// The context's checkpoint writer thread and its one-slot job queue: at most
+// one write is queued or running at a time.
+struct WriterState {
+    std::thread thread;
+    std::mutex mu;
+    std::condition_variable cv;
+    bool started = false, stop = false;
+    bool pending = false, running = false;  // a job queued / being written
+    // the job
+    std::string dir;
+    int32_t step = -1;
+    // result of the last finished job
+    bool have_result = false, collected = true;
+    int status = ADAMW_OK;
+    std::string error, path;
+};
+
+}  // namespace osr
+
+struct adamw_ctx {
+    int64_t n = 0;
+    std::vector<int64_t> offsets, numels;
+    int device = -1;
+    int sm_count = 0;
+    osr::KernelCaps caps{};
+    double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
+
+    // norm scratch: [NormResult | counter | pad][partials x kNormBlocksMax]
+    unsigned char* d_scratch = nullptr;
+    osr::NormResult* d_res = nullptr;
+    unsigned int* d_counter = nullptr;
+    double* d_partials = nullptr;
+    osr::NormResult* h_res = nullptr;      // pinned, mapped: host view
+    osr::NormResult* h_res_dev = nullptr;  // device view of the same memory
+    cudaEvent_t ev_norm = nullptr;
+    bool norm_launched = false;
+    cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
+
+    // Checkpoint staging.  Device image at alloc + 8, so that its w region
+    // (image + 8) starts on a 16-byte boundary for the pack kernel's vector
+    // stores; pinned host image at the (page-aligned) start of its
+    // allocation, padded to a whole number of 4 KiB blocks, so that the
+    // writer can hand it to the disk with O_DIRECT.
+    bool has_ckpt = false;
+    unsigned char* d_image_alloc = nullptr;
+    unsigned char* h_image_alloc = nullptr;
+    cudaEvent_t ev_pack = nullptr, ev_d2h = nullptr;
+    bool packed = false, d2h_pending = false;
+    int32_t packed_step = -1;
+
+    // Checkpoint writing: options and the writer thread.
+    int32_t keep = 0;                   // rotation: newest files kept (0 = all)
+    int32_t write_flags = osr::kWriteDirect;
+    osr::WriterState writer;
+
+    unsigned char* d_image() const { return d_image_alloc + 8; }
+    unsigned char* h_image() const { return h_image_alloc; }
+    size_t image_bytes() const { return size_t(8 + 12 * n); }
+    size_t h_image_capacity() const { return osr::round_up_block(image_bytes()); }
+};
+
+
+namespace osr {
+// Waits (host side) until the context's writer holds no job; afterwards the
+// pinned image may be overwritten.  No-op when no writer thread was started.
+void writer_drain(adamw_ctx* c);
+// Lets the writer finish its queued job, then joins the thread.
+void writer_stop(adamw_ctx* c);
+}  // namespace osr

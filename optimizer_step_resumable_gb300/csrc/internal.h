@@ -78,12 +78,23 @@ int launch_pack(const float* w, const float* m, const float* v, int64_t n,
                 void* stream);
 
 // Host file I/O (ckpt_io.cpp).
+constexpr size_t kIoBlock = 4096;  // O_DIRECT alignment of address, length and offset
+inline size_t round_up_block(size_t b) { return (b + kIoBlock - 1) / kIoBlock * kIoBlock; }
+constexpr int32_t kWriteDirect = 1;  // try O_DIRECT (falls back when refused)
+
 struct IoPiece {
     const void* data;
     size_t bytes;
+    size_t capacity;  // readable bytes at data (>= bytes); O_DIRECT needs
+                      // round_up_block(bytes)
 };
+// Writes the pieces, in order, to <dir>/step_%06d.bin atomically.  With
+// kWriteDirect and a single 4 KiB-aligned piece of enough capacity, the data
+// goes to the disk with O_DIRECT (whole blocks, then ftruncate to size).
 int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
-                      int npieces, char* path_out, size_t path_cap);
+                      int npieces, char* path_out, size_t path_cap, int32_t flags = 0);
+// Deletes all but the `keep` newest step_<digits>.bin files of dir.
+int rotate_files(const char* dir, int32_t keep, int32_t* removed);
 // Validates header and size; on success *fd_out is an open descriptor
 // positioned after the header (caller closes it).
 int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
