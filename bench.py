@@ -249,6 +249,7 @@ def run_ours(args):
 
     import optimizer_step_resumable_gb300 as osr
     from optimizer_step_resumable_gb300 import build as lib_build
+    from optimizer_step_resumable_gb300 import sharded
     from synthetic import device as synth_dev
 
     lib_build.build()  # no-op when the library is up to date
@@ -281,9 +282,28 @@ def run_ours(args):
         osr.ckpt_pack(ctx, step, w, m, v, main_stream=main, side_stream=side)
         osr.ckpt_write_async(ctx, ckdir)
 
+    def step(t, ev=None):
+        """One optimizer step (single GPU: norm + fused kernel; N ranks: each
+        rank owns one shard of an N x n state, the shards' sums of squares
+        are exchanged and added in rank order, then the fused update)."""
+        if world == 1:
+            if ev is not None:
+                osr.adamw_record_events(ctx, *ev)
+            osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+            return
+        if ev is not None:
+            ev[0].record(main)
+        local = osr.grad_sumsq(ctx, g)
+        if ev is not None:
+            ev[1].record(main)
+        total = sharded.global_sumsq(local)
+        osr.adamw_clip_step_ex(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip, global_sumsq=total)
+        if ev is not None:
+            ev[2].record(main)
+
     t = 1
     for _ in range(W):
-        osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+        step(t)
         t += 1
     checkpoint(t - 1)
     osr.ckpt_wait(ctx)
@@ -305,8 +325,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     start.record(main)
     for k in range(K):
-        osr.adamw_record_events(ctx, *evs[k])
-        osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+        step(t, evs[k])
         if k in ck_steps:
             a, b, c = pack_ev[k]
             a.record(main)
@@ -345,8 +364,9 @@ def run_ours(args):
         e_start.record(main)
         for k in range(K):
             g.copy_(g_host, non_blocking=True)
-            osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
-            osr.adamw_last_norm(ctx)
+            step(t)
+            if world == 1:
+                osr.adamw_last_norm(ctx)
             if k in ck_steps:
                 checkpoint(t)
             t += 1
@@ -375,7 +395,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": wl.name, "n_params": n, "tensors": len(off),
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "parallelism": (f"zero1 x{world}: one {wl.name} shard per rank, sums of squares "
+                            f"exchanged (gloo) and added in rank order each step")
+                           if world > 1 else "single GPU",
             "ckpt_every": C, "ckpts_timed": len(ck_steps),
             "ckpt_bytes": 8 + 12 * n,
             "l2": f"inputs larger than L2: w, g, m, v = {16 * n / 1e9:.2f} GB",

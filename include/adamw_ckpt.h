@@ -66,6 +66,9 @@ extern "C" {
 /* adamw_create flags. */
 #define ADAMW_CREATE_NO_CKPT 1 /* do not allocate the checkpoint staging    */
 
+/* adamw_clip_step_ex flags. */
+#define ADAMW_ZERO_GRAD 1 /* write 0 into g after reading it                */
+
 /* ckpt_set_options / ckpt_write_image flags. */
 #define CKPT_DIRECT 1 /* write with O_DIRECT when the file system allows it */
 
@@ -146,10 +149,45 @@ ADAMW_API int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, floa
                     void* stream);
 
 /*
+ * adamw_clip_step with the two extensions a training loop needs around it.
+ *
+ * Gradient accumulation ([B] "Accumulation across micro-batches": backward
+ * adds into the gradient buffer, then scale_grads(1 / n_micro), the optimizer
+ * step, zero_grads): grad_scale > 0 multiplies the gradient before the norm,
+ * the clip and the update, folded into the clip factor at no extra traffic;
+ * flags ADAMW_ZERO_GRAD makes the fused kernel write 0 into d_g after reading
+ * it (+4 bytes per parameter; a skipped non-finite step leaves g as is).
+ *
+ * Sharded state (ZeRO-1 style: each rank owns one contiguous range of the
+ * flat state and holds the gradient of that range): global_sumsq >= 0 is the
+ * sum of g^2 of the whole raw gradient -- the ranks' grad_sumsq values,
+ * summed in rank order -- and replaces the local reduction: no norm kernel
+ * runs, the clip factor is computed on the host in double, and a non-finite
+ * global norm returns ADAMW_ENONFINITE at once with nothing launched.
+ * global_sumsq < 0 reduces this context's gradient on the GPU, as
+ * adamw_clip_step does (which is this call with grad_scale 1,
+ * global_sumsq -1, flags 0).
+ */
+ADAMW_API int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m,
+                                 float* d_v, int32_t t, double lr, double wd,
+                                 double clip, double grad_scale, double global_sumsq,
+                                 int32_t flags, void* stream);
+
+/*
+ * Sum of g^2 over this context's n values of d_g (double, the same
+ * deterministic two-level reduction as grad_global_norm); waits for the
+ * stream.  For a sharded state, each rank's value is exchanged and summed in
+ * rank order to give adamw_clip_step_ex's global_sumsq.  Returns
+ * ADAMW_ENONFINITE (with the inf/nan sum stored) if the sum is not finite.
+ */
+ADAMW_API int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream);
+
+/*
  * Waits for the last norm reduction launched on this context (by
  * grad_global_norm or adamw_clip_step) and reports it: *norm_out (may be
- * NULL) receives ||g||_2 in double, *scale_out (may be NULL) the clip factor
- * that step applied.  Returns ADAMW_ENONFINITE if the norm was inf/nan (the
+ * NULL) receives the norm of the (scaled) gradient in double, *scale_out
+ * (may be NULL) the factor that step applied to the raw gradient
+ * (grad_scale times the clip factor).  Returns ADAMW_ENONFINITE if the norm was inf/nan (the
  * step, if any, was skipped), ADAMW_ESTATE if no reduction ran yet.
  */
 ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out);

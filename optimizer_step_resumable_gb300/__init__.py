@@ -21,6 +21,7 @@ OK = 0
 EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9, -1)
 CREATE_NO_CKPT = 1
 CKPT_DIRECT = 1
+ZERO_GRAD = 1
 CKPT_REQ_WRITE, CKPT_REQ_EXIT = 1, 2
 CKPT_ACTION_NONE, CKPT_ACTION_WRITING, CKPT_ACTION_EXIT = 0, 1, 2
 
@@ -38,6 +39,10 @@ SIGNATURES = {
     "adamw_clip_step": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _c.c_int32, _c.c_double,
                                    _c.c_double, _c.c_double, _vp]),
     "adamw_last_norm": (_c.c_int, [_vp, _c.POINTER(_c.c_double), _c.POINTER(_c.c_float)]),
+    "adamw_clip_step_ex": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _c.c_int32, _c.c_double,
+                                      _c.c_double, _c.c_double, _c.c_double, _c.c_double,
+                                      _c.c_int32, _vp]),
+    "grad_sumsq": (_c.c_int, [_vp, _vp, _c.POINTER(_c.c_double), _vp]),
     "adamw_record_events": (_c.c_int, [_vp, _vp, _vp, _vp]),
     "adamw_clip_step_noalloc": (_c.c_int, [_vp, _vp, _vp, _vp, _c.c_int64, _c.c_int32,
                                            _c.c_double, _c.c_double, _c.c_double,
@@ -205,6 +210,28 @@ def adamw_clip_step(ctx: Context, w, g, m, v, t: int, lr: float, wd: float,
                                    _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), int(t),
                                    float(lr), float(wd), float(clip), _stream(stream))
     _check(st, "adamw_clip_step")
+
+
+def adamw_clip_step_ex(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, clip: float,
+                       grad_scale: float = 1.0, global_sumsq: float = -1.0,
+                       zero_grad: bool = False, stream=None):
+    """adamw_clip_step with a gradient scale (micro-batch averaging), an
+    optional global sum of squares (sharded state) and ZERO_GRAD."""
+    n = ctx.n
+    st = library().adamw_clip_step_ex(
+        ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"), _dev_ptr(m, n, "m"),
+        _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip), float(grad_scale),
+        float(global_sumsq), ZERO_GRAD if zero_grad else 0, _stream(stream))
+    _check(st, "adamw_clip_step_ex")
+
+
+def grad_sumsq(ctx: Context, g, stream=None) -> float:
+    """Sum of g^2 over the context's n values (waits); raises NonFiniteGradient."""
+    out = ctypes.c_double()
+    st = library().grad_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g"), ctypes.byref(out),
+                              _stream(stream))
+    _check(st, "grad_sumsq")
+    return out.value
 
 
 def adamw_last_norm(ctx: Context):

@@ -117,10 +117,11 @@ int validate_table(int64_t n, const int64_t* offsets, const int64_t* numels, int
     return ADAMW_OK;
 }
 
-int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream)
+int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream,
+                   double grad_scale = 1.0)
 {
     const int e = osr::launch_norm(g, c->n, clip, c->d_partials, c->d_counter, c->d_res,
-                                   c->h_res_dev, stream);
+                                   c->h_res_dev, stream, grad_scale);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "norm kernel launch");
     CUDA_TRY(cudaEventRecord(c->ev_norm, static_cast<cudaStream_t>(stream)));
@@ -279,6 +280,14 @@ int grad_global_norm(adamw_ctx* ctx, const float* d_g, double* h_norm, void* str
 int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, float* d_v,
                     int32_t t, double lr, double wd, double clip, void* stream)
 {
+    return adamw_clip_step_ex(ctx, d_w, const_cast<float*>(d_g), d_m, d_v, t, lr, wd, clip, 1.0,
+                              -1.0, 0, stream);
+}
+
+int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float* d_v,
+                       int32_t t, double lr, double wd, double clip, double grad_scale,
+                       double global_sumsq, int32_t flags, void* stream)
+{
     osr::clear_error();
     if (!ctx)
         return fail(ADAMW_EINVAL, "ctx is NULL");
@@ -292,6 +301,11 @@ int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, fl
         return fail(ADAMW_EINVAL, "lr=%g wd=%g must be finite and >= 0", lr, wd);
     if (!(clip > 0.0))
         return fail(ADAMW_EINVAL, "clip=%g must be > 0 (INFINITY disables clipping)", clip);
+    if (!(grad_scale > 0.0 && std::isfinite(grad_scale)))
+        return fail(ADAMW_EINVAL, "grad_scale=%g must be finite and > 0", grad_scale);
+    if (flags & ~ADAMW_ZERO_GRAD)
+        return fail(ADAMW_EINVAL, "unknown flags 0x%x", flags);
+    const bool external = !(global_sumsq < 0.0);  // NaN counts as given (non-finite)
 
     // Bias-correction and decay scalars, in double on the host, rounded to
     // float once.
@@ -306,6 +320,15 @@ int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, fl
     k.step_size = float(lr / bc1);
     k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
     k.decay = float(1.0 - lr * wd);
+    k.scale = 1.0f;
+    if (external) {
+        // the global norm of the sharded gradient, from the ranks' sums
+        const double norm = grad_scale * std::sqrt(global_sumsq);
+        if (!std::isfinite(norm))
+            return fail(ADAMW_ENONFINITE, "global gradient norm is %g: the update was skipped",
+                        norm);
+        k.scale = float(grad_scale * (norm > clip ? clip / norm : 1.0));
+    }
 
     DeviceScope scope(ctx->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -313,17 +336,37 @@ int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, fl
     ctx->prof[0] = ctx->prof[1] = ctx->prof[2] = nullptr;
     if (prof[0])
         CUDA_TRY(cudaEventRecord(prof[0], st));
-    rc = launch_norm_on(ctx, d_g, clip, stream);
-    if (rc != ADAMW_OK)
-        return rc;
+    if (!external) {
+        rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale);
+        if (rc != ADAMW_OK)
+            return rc;
+    }
     if (prof[1])
         CUDA_TRY(cudaEventRecord(prof[1], st));
-    const int e = osr::launch_adamw(d_w, d_g, d_m, d_v, ctx->n, k, ctx->d_res, ctx->caps, stream);
+    const int e = osr::launch_adamw(d_w, d_g, d_m, d_v, ctx->n, k, external ? nullptr : ctx->d_res,
+                                    ctx->caps, stream, (flags & ADAMW_ZERO_GRAD) != 0);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "clip+AdamW kernel launch");
     if (prof[2])
         CUDA_TRY(cudaEventRecord(prof[2], st));
     return ADAMW_OK;
+}
+
+int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !h_sumsq)
+        return fail(ADAMW_EINVAL, "ctx or h_sumsq is NULL");
+    int rc = check_state_ptr(d_g, "d_g");
+    if (rc != ADAMW_OK)
+        return rc;
+    DeviceScope scope(ctx->device);
+    rc = launch_norm_on(ctx, d_g, INFINITY, stream);
+    if (rc != ADAMW_OK)
+        return rc;
+    rc = read_norm(ctx, nullptr, nullptr);
+    *h_sumsq = static_cast<const volatile osr::NormResult*>(ctx->h_res)->sumsq;
+    return rc;
 }
 
 int adamw_record_events(adamw_ctx* ctx, void* ev_begin, void* ev_mid, void* ev_end)

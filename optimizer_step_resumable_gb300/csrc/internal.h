@@ -22,9 +22,9 @@ const char* last_error_text();
 // host mirror (read by adamw_last_norm without a copy).
 // ---------------------------------------------------------------------------
 struct NormResult {
-    double sumsq;       // sum of g_i^2 (fixed-order, double)
-    double norm;        // sqrt(sumsq)
-    float scale;        // clip factor: norm > clip ? clip / norm : 1
+    double sumsq;       // sum of g_i^2 of the raw gradient (fixed-order, double)
+    double norm;        // grad_scale * sqrt(sumsq): the norm of the scaled gradient
+    float scale;        // factor applied to raw g: grad_scale * clip factor
     int32_t nonfinite;  // 1 if norm is inf or nan (the step is skipped)
     uint32_t seq;       // incremented by every reduction (host staleness check)
     uint32_t pad;
@@ -38,6 +38,7 @@ struct StepScalars {
     float step_size;        // lr / (1 - beta1^t)
     float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
     float decay;            // 1 - lr * wd
+    float scale;            // gradient factor when no norm result is read
 };
 
 // Tunables of the kernels (fixed at compile time; see kernels.cu).
@@ -67,12 +68,14 @@ struct KernelCaps {
 // Kernel launchers (norm.cu, step.cu, pack.cu).  All return cudaError_t as int.
 int query_step_caps(int sm_count, KernelCaps* caps);
 int query_pack_caps(int sm_count, KernelCaps* caps);
+// The norm kernel publishes norm = grad_scale sqrt(sum g^2) and the factor
+// applied to g: grad_scale * (norm > clip ? clip / norm : 1).
 int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream);
+                void* stream, double grad_scale = 1.0);
 int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res,
-                 const KernelCaps& caps, void* stream);
+                 const KernelCaps& caps, void* stream, bool zero_grad = false);
 int launch_pack(const float* w, const float* m, const float* v, int64_t n,
                 int32_t step, unsigned char* image, const KernelCaps& caps,
                 void* stream);

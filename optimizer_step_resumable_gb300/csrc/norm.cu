@@ -85,7 +85,7 @@ __device__ __forceinline__ double run_sumsq(const float4 (&x)[U])
 // ---------------------------------------------------------------------------
 template <bool kVec>
 __global__ void __launch_bounds__(kNormThreads)
-    k_grad_norm(const float* __restrict__ g, int64_t n, double clip,
+    k_grad_norm(const float* __restrict__ g, int64_t n, double clip, double grad_scale,
                 double* __restrict__ partials, unsigned int* __restrict__ counter,
                 NormResult* __restrict__ d_res, NormResult* h_res)
 {
@@ -142,10 +142,12 @@ __global__ void __launch_bounds__(kNormThreads)
     if (tid == 0) {
         NormResult r;
         r.sumsq = s;
-        r.norm = sqrt(s);
+        // the norm of the scaled gradient grad_scale * g, and the factor
+        // applied to raw g (grad_scale times the clip factor), rounded once
+        r.norm = grad_scale * sqrt(s);
         const bool finite = isfinite(r.norm);
         r.nonfinite = finite ? 0 : 1;
-        r.scale = (finite && r.norm > clip) ? float(clip / r.norm) : 1.0f;
+        r.scale = float(grad_scale * ((finite && r.norm > clip) ? clip / r.norm : 1.0));
         r.seq = d_res->seq + 1u;
         r.pad = 0;
         *d_res = r;
@@ -166,16 +168,16 @@ __global__ void __launch_bounds__(kNormThreads)
 
 int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream)
+                void* stream, double grad_scale)
 {
     const int blocks = norm_blocks(n);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (detail::aligned16(g))
-        k_grad_norm<true><<<blocks, kNormThreads, 0, s>>>(g, n, clip, partials, counter,
-                                                           d_res, h_res_dev);
+        k_grad_norm<true><<<blocks, kNormThreads, 0, s>>>(g, n, clip, grad_scale, partials,
+                                                           counter, d_res, h_res_dev);
     else
-        k_grad_norm<false><<<blocks, kNormThreads, 0, s>>>(g, n, clip, partials, counter,
-                                                            d_res, h_res_dev);
+        k_grad_norm<false><<<blocks, kNormThreads, 0, s>>>(g, n, clip, grad_scale, partials,
+                                                            counter, d_res, h_res_dev);
     return int(cudaGetLastError());
 }
 

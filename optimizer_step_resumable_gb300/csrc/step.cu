@@ -57,23 +57,33 @@ constexpr int kStepVec = 2;  // float4 of each array per thread per chunk
 
 // Reads w, g, m, v once and writes w, m, v once (28 bytes per parameter).
 // The clip factor and the non-finite flag come from the norm kernel's
-// result in device memory, so nothing returns to the host between kernels.
-template <bool kVec>
+// result in device memory, so nothing returns to the host between kernels;
+// with res == nullptr the factor is k.scale (the host computed it from a
+// global sum of squares).  kZero also writes 0 into g after reading it
+// ("zero_grads" for the next accumulation), +4 bytes per parameter.
+template <bool kVec, bool kZero>
 __global__ void __launch_bounds__(kStepThreads)
     k_clip_adamw(float* __restrict__ w, const float* __restrict__ g,
                  float* __restrict__ m, float* __restrict__ v, int64_t n,
                  StepScalars k, const NormResult* __restrict__ res)
 {
-    if (res->nonfinite)
-        return;
-    const float s = res->scale;
+    float s = k.scale;
+    if (res) {
+        if (res->nonfinite)
+            return;
+        s = res->scale;
+    }
+    // written through the same restrict pointer it is read from
+    float* const gw = const_cast<float*>(g);
     const int64_t gtid = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
     const int64_t stride = int64_t(gridDim.x) * kStepThreads;
     if (kVec) {
         float4* w4 = reinterpret_cast<float4*>(w);
         const float4* g4 = reinterpret_cast<const float4*>(g);
+        float4* gw4 = reinterpret_cast<float4*>(gw);
         float4* m4 = reinterpret_cast<float4*>(m);
         float4* v4 = reinterpret_cast<float4*>(v);
+        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
         const int64_t n4 = n >> 2;
         constexpr int64_t chunk = int64_t(kStepThreads) * kStepVec;
         const int64_t nchunks = n4 / chunk;
@@ -97,6 +107,8 @@ __global__ void __launch_bounds__(kStepThreads)
                 __stcs(w4 + i, W[j]);
                 __stcs(m4 + i, M[j]);
                 __stcs(v4 + i, V[j]);
+                if (kZero)
+                    __stcs(gw4 + i, zero4);
             }
         }
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
@@ -106,6 +118,8 @@ __global__ void __launch_bounds__(kStepThreads)
             __stcs(w4 + i, W);
             __stcs(m4 + i, M);
             __stcs(v4 + i, V);
+            if (kZero)
+                __stcs(gw4 + i, zero4);
         }
         if (gtid < (n & 3)) {
             const int64_t e = (n4 << 2) + gtid;
@@ -114,6 +128,8 @@ __global__ void __launch_bounds__(kStepThreads)
             w[e] = W;
             m[e] = M;
             v[e] = V;
+            if (kZero)
+                gw[e] = 0.0f;
         }
     } else {
         for (int64_t e = gtid; e < n; e += stride) {
@@ -122,6 +138,8 @@ __global__ void __launch_bounds__(kStepThreads)
             __stcs(w + e, W);
             __stcs(m + e, M);
             __stcs(v + e, V);
+            if (kZero)
+                __stcs(gw + e, 0.0f);
         }
     }
 }
@@ -130,29 +148,37 @@ __global__ void __launch_bounds__(kStepThreads)
 
 int query_step_caps(int sm_count, KernelCaps* caps)
 {
-    caps->step_vec = detail::resident_blocks(reinterpret_cast<const void*>(&k_clip_adamw<true>),
-                                             kStepThreads, sm_count);
+    // the zeroing variants have the same shape; their counts are not needed
+    caps->step_vec = detail::resident_blocks(
+        reinterpret_cast<const void*>(&k_clip_adamw<true, false>), kStepThreads, sm_count);
     caps->step_scalar = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<false>), kStepThreads, sm_count);
+        reinterpret_cast<const void*>(&k_clip_adamw<false, false>), kStepThreads, sm_count);
     return int(cudaGetLastError());
 }
 
 int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res, const KernelCaps& caps,
-                 void* stream)
+                 void* stream, bool zero_grad)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool vec = detail::aligned16(w) && detail::aligned16(g) && detail::aligned16(m) && detail::aligned16(v);
+    const bool vec = detail::aligned16(w) && detail::aligned16(g) && detail::aligned16(m) &&
+                     detail::aligned16(v);
     if (vec) {
         const int cap = caps.step_vec;
         const int64_t want = detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        k_clip_adamw<true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+        if (zero_grad)
+            k_clip_adamw<true, true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+        else
+            k_clip_adamw<true, false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
     } else {
         const int cap = caps.step_scalar;
         const int64_t want = detail::ceil_div(n, kStepThreads);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        k_clip_adamw<false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+        if (zero_grad)
+            k_clip_adamw<false, true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+        else
+            k_clip_adamw<false, false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
     }
     return int(cudaGetLastError());
 }

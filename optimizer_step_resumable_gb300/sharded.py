@@ -1,0 +1,63 @@
+"""Sharded (ZeRO-1 style) optimizer step: host-side partition and exchange.
+
+Each rank owns one contiguous range of the flat state (its shard of w, m, v
+and the gradient of that range).  The global clip needs the norm of the
+whole gradient, so the ranks exchange their shards' sums of squares -- one
+double each -- and add them in rank order, which makes the result the same
+on every rank and from run to run.  Each rank then runs the fused update on
+its own shard with that global sum (adamw_clip_step_ex, global_sumsq).  The
+exchange uses torch.distributed (gloo or NCCL); everything else runs in the
+library's kernels.
+"""
+from __future__ import annotations
+
+from . import adamw_clip_step_ex, grad_sumsq
+
+
+def shard_range(n: int, rank: int, world: int, align: int = 4):
+    """(offset, numel) of rank's contiguous shard of [0, n): equal shards of
+    a multiple of `align` elements (16-byte boundaries for float32), the
+    remainder on the last rank."""
+    if world < 1 or not 0 <= rank < world or n < world:
+        raise ValueError("need 0 <= rank < world <= n")
+    base = (n // world) // align * align
+    if base == 0:
+        base = n // world
+    off = rank * base
+    numel = n - off if rank == world - 1 else base
+    return off, numel
+
+
+def ordered_sum(parts):
+    """Sum of the ranks' values in rank order, in double."""
+    total = 0.0
+    for x in parts:
+        total = total + float(x)
+    return total
+
+
+def global_sumsq(local: float, group=None) -> float:
+    """Every rank's local sum of squares, gathered and added in rank order."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return float(local)
+    world = dist.get_world_size(group)
+    backend = dist.get_backend(group)
+    device = (torch.device("cuda", torch.cuda.current_device())
+              if backend == "nccl" else torch.device("cpu"))
+    mine = torch.tensor([float(local)], dtype=torch.float64, device=device)
+    parts = [torch.empty_like(mine) for _ in range(world)]
+    dist.all_gather(parts, mine, group=group)
+    return ordered_sum(p.item() for p in parts)
+
+
+def sharded_clip_step(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=1.0, zero_grad=False,
+                      group=None, stream=None):
+    """One clipped-AdamW step on this rank's shard; returns the global sum
+    of squares of the raw gradient."""
+    local = grad_sumsq(ctx, g, stream=stream)
+    total = global_sumsq(local, group)
+    adamw_clip_step_ex(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=grad_scale,
+                       global_sumsq=total, zero_grad=zero_grad, stream=stream)
+    return total

@@ -91,6 +91,11 @@ class Oracle:
             c.c_double, c.c_double, c.c_double, c.c_double, c.c_double,
             c.POINTER(c.c_double)]
         lib.oracle_adamw_clip_step.restype = c.c_int
+        lib.oracle_adamw_clip_step_scaled.argtypes = [
+            _f32p, _f32p, _f32p, _f32p, c.c_int64, c.c_int32, c.c_double,
+            c.c_double, c.c_double, c.c_double, c.c_double, c.c_double,
+            c.c_double, c.POINTER(c.c_double)]
+        lib.oracle_adamw_clip_step_scaled.restype = c.c_int
         lib.oracle_adamw_at.argtypes = [
             _i64p, c.c_int64, _f32p, _f32p, _f32p, _f32p, c.c_double,
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
@@ -153,6 +158,21 @@ class Oracle:
             float(beta1), float(beta2), float(eps), ctypes.byref(norm))
         if st not in (OK, ENONFINITE) or (st != OK and raise_on_error):
             raise OracleError(st, "oracle_adamw_clip_step")
+        return st, norm.value
+
+    def adamw_clip_step_scaled(self, w, g, m, v, t, lr, wd, clip, grad_scale,
+                               beta1=BETA1, beta2=BETA2, eps=EPS, raise_on_error=True):
+        """In-place step on grad_scale * g (gradient accumulation)."""
+        for a in (w, m, v):
+            _check_inplace(a)
+        g = _f32(g)
+        norm = ctypes.c_double()
+        st = self._lib.oracle_adamw_clip_step_scaled(
+            w, g, m, v, w.size, int(t), float(lr), float(wd), float(clip),
+            float(grad_scale), float(beta1), float(beta2), float(eps),
+            ctypes.byref(norm))
+        if st not in (OK, ENONFINITE) or (st != OK and raise_on_error):
+            raise OracleError(st, "oracle_adamw_clip_step_scaled")
         return st, norm.value
 
     def adamw_at(self, idx, w, g, m, v, s, t, lr, wd, beta1=BETA1,

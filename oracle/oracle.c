@@ -158,6 +158,44 @@ int oracle_adamw_clip_step(float* w, const float* g, float* m, float* v,
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------
+ * The step after gradient accumulation.  "Grow a Language Model: Backprop"
+ * (unhomeschool.com), section "Accumulation across micro-batches": backward
+ * adds each micro-batch's gradient into the buffer, scale_grads(1/n_micro)
+ * averages it, then the optimizer step runs (and zero_grads clears the
+ * buffer).  Here every gradient value is first multiplied by grad_scale in
+ * double; the norm, the clip and the update then see the scaled vector.
+ * ---------------------------------------------------------------------- */
+int oracle_adamw_clip_step_scaled(float* w, const float* g, float* m, float* v,
+                                  int64_t n, int32_t t, double lr, double wd,
+                                  double clip, double grad_scale, double beta1,
+                                  double beta2, double eps, double* norm_out)
+{
+    if (n < 0 || t < 1)
+        return OR_EINVAL;
+    double sumsq = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double x = (double)g[i] * grad_scale;
+        sumsq = sumsq + x * x;
+    }
+    double norm = sqrt(sumsq);
+    if (norm_out)
+        *norm_out = norm;
+    if (!isfinite(norm))
+        return OR_ENONFINITE;
+    double s = oracle_clip_scale(norm, clip);
+    for (int64_t i = 0; i < n; ++i) {
+        oracle_terms r;
+        oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,
+                             (double)m[i], (double)v[i], s, t, lr, wd, beta1,
+                             beta2, eps, &r);
+        w[i] = (float)r.w;
+        m[i] = (float)r.m;
+        v[i] = (float)r.v;
+    }
+    return OR_OK;
+}
+
 /* The same update at chosen indices only, given the clip factor s (from a
  * full-vector norm computed separately).  Used to check outputs of a large
  * state one element at a time.  Results go to the *_out arrays. */

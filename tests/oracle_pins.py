@@ -289,6 +289,52 @@ def pin_step_matches_elements(o, tmp):
     assert v.tobytes() == vs.tobytes()
 
 
+def pin_scaled_step_power_of_two(o, tmp):
+    """Scaling the gradient by 2^-k is exact: the scaled step equals the
+    plain step on g * 2^-k, bit for bit (norm, state)."""
+    rng = np.random.default_rng(9)
+    n = 300
+    g = rng.normal(0, 3.0, n).astype(np.float32)
+    for gs in (0.5, 0.25, 2.0 ** -7):
+        a = [rng.normal(0, 0.02, n).astype(np.float32), np.zeros(n, np.float32),
+             np.zeros(n, np.float32)]
+        b = [x.copy() for x in a]
+        _, n1 = o.adamw_clip_step_scaled(*a[:1], g, *a[1:], 1, 3e-3, 0.01, 1.0, gs)
+        _, n2 = o.adamw_clip_step(b[0], g * np.float32(gs), b[1], b[2], 1, 3e-3, 0.01, 1.0)
+        assert n1 == n2
+        for x, y in zip(a, b):
+            assert x.tobytes() == y.tobytes()
+
+
+def pin_scaled_step_clips_the_scaled_norm(o, tmp):
+    """The clip sees the averaged gradient: [3, 4] scaled by 1/4 has norm
+    1.25 < 2 (no clip, m = 0.1 * 0.75 at t = 1); [30, 40] scaled by 1/2 has
+    norm 25 > 1 (factor 1/25: g_hat = [0.6, 0.8])."""
+    for g, gs, c, want_norm, want_m in (([3, 4], 0.25, 2.0, 1.25, [0.075, 0.1]),
+                                        ([30, 40], 0.5, 1.0, 25.0, [0.06, 0.08])):
+        w = np.zeros(2, np.float32)
+        m = np.zeros(2, np.float32)
+        v = np.zeros(2, np.float32)
+        _, norm = o.adamw_clip_step_scaled(w, np.array(g, np.float32), m, v, 1, 0.1, 0.0, c, gs)
+        assert norm == want_norm
+        assert np.allclose(m, np.array(want_m, np.float32), rtol=2 ** -23, atol=0)
+
+
+def pin_micro_batch_average(o, tmp):
+    """Accumulating k micro-batch gradients and scaling by 1/k is the step on
+    their mean (small integers: the sums and the 1/4 are exact)."""
+    rng = np.random.default_rng(10)
+    parts = [rng.integers(-8, 9, 64).astype(np.float32) for _ in range(4)]
+    acc = np.sum(parts, axis=0).astype(np.float32)
+    mean = (acc / np.float32(4)).astype(np.float32)
+    a = [np.full(64, 0.5, np.float32), np.zeros(64, np.float32), np.zeros(64, np.float32)]
+    b = [x.copy() for x in a]
+    o.adamw_clip_step_scaled(a[0], acc, a[1], a[2], 2, 0.01, 0.1, 5.0, 0.25)
+    o.adamw_clip_step(b[0], mean, b[1], b[2], 2, 0.01, 0.1, 5.0)
+    for x, y in zip(a, b):
+        assert x.tobytes() == y.tobytes()
+
+
 # --- checkpoint format -----------------------------------------------------
 
 def pin_ckpt_printed_sizes(o, tmp):

@@ -61,6 +61,12 @@ MUTANTS = {
     "step_rounds_m_from_v": ("m[i] = (float)r.m;", "m[i] = (float)r.v;"),
     "step_t_off_by_one": ("double s = oracle_clip_scale(norm, clip);",
                           "double s = oracle_clip_scale(norm, clip);\n    t = t + 1;"),
+    "scaled_clip_on_raw_norm": ("double x = (double)g[i] * grad_scale;\n        sumsq = sumsq + x * x;",
+                                "double x = (double)g[i];\n        sumsq = sumsq + x * x;"),
+    "scaled_update_unscaled": ("oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,",
+                               "oracle_adamw_element((double)w[i], (double)g[i],"),
+    "scaled_twice": ("double x = (double)g[i] * grad_scale;",
+                     "double x = (double)g[i] * grad_scale * grad_scale;"),
 }
 
 
@@ -85,7 +91,8 @@ def _pins_fail(o, tmp_path):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, source, tmp_path):
     old, new = MUTANTS[name]
-    assert source.count(old) == 1, f"mutation anchor not unique/found: {old!r}"
+    # planted wherever the anchor occurs (the same mistake made consistently)
+    assert source.count(old) >= 1, f"mutation anchor not found: {old!r}"
     src = tmp_path / "mutant.c"
     src.write_text(source.replace(old, new))
     lib = str(tmp_path / "mutant.so")
