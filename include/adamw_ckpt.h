@@ -357,6 +357,60 @@ ADAMW_API int ckpt_write_image(const char* dir, const void* image, int64_t bytes
                                size_t path_cap);
 ADAMW_API int ckpt_rotate(const char* dir, int32_t keep, int32_t* removed);
 
+/*
+ * Sharded checkpoint ([S]: each rank writes its own shard file, a manifest
+ * records which rank owns which range).  One directory per checkpoint:
+ *   <dir>/step_NNNNNN/rank<R>.bin    shard R in the step_NNNNNN.bin format
+ *                                    over its range (its own n in the header)
+ *   <dir>/step_NNNNNN/manifest.json  {"world_size", "step",
+ *       "wall_clock_seconds", "shards": [{"rank", "path", "sha256",
+ *       "param_shard_offset", "param_shard_numel"}], "schema_version": 1}
+ * ([S] "Manifest schema").  Every rank writes and fsyncs its file under
+ * <dir>/step_NNNNNN.tmp/ and reports its sha256; once all have (the caller
+ * synchronises the ranks and gathers the digests), rank 0 calls
+ * ckpt_manifest_commit, which writes the manifest there (tmp, fsync, rename),
+ * fsyncs, and renames the directory to step_NNNNNN: the checkpoint appears
+ * complete or not at all ([S] "Atomic write"; one directory rename instead
+ * of one rename per file, so the set is atomic).  Loading refuses
+ * ([S] "Three failure modes"): a world size other than expected_world
+ * (ADAMW_EMISMATCH), a shard count or rank set that does not match
+ * world_size (ADAMW_EMISMATCH), a shard whose size, header or sha256
+ * disagrees with the manifest (ADAMW_ESIZE / ADAMW_EFORMAT).
+ *
+ * ckpt_shard_write: writes the image of the last ckpt_pack of this context
+ * (its shard, step = the packed step) as rank<rank>.bin; sha256_hex_out
+ * receives 64 hex digits + NUL.  Blocks until durable.
+ * ckpt_shard_write_host: the same from host arrays of n floats.
+ * ckpt_manifest_commit: rank 0, after every shard is written; offsets,
+ * numels: per rank, contiguous from 0; sha256_hex: the ranks' digests
+ * concatenated (64 x world hex digits).  path_out receives the directory.
+ * ckpt_manifest_load: validates a step directory (digests too if
+ * verify_sha256) and returns its step, world size and layout (cap entries).
+ * ckpt_shard_read: validates the manifest and this rank's shard (size,
+ * header, sha256), then copies the shard into d_w, d_m, d_v (n = the
+ * context's n must equal the shard's numel) and waits; the device arrays
+ * are untouched on failure.
+ */
+ADAMW_API int ckpt_shard_write(adamw_ctx* ctx, const char* dir, int32_t rank,
+                               char* sha256_hex_out);
+ADAMW_API int ckpt_shard_write_host(const char* dir, int32_t step, int32_t rank, int32_t n,
+                                    const float* h_w, const float* h_m, const float* h_v,
+                                    char* sha256_hex_out);
+ADAMW_API int ckpt_manifest_commit(const char* dir, int32_t step, int32_t world,
+                                   double wall_clock_seconds, const int64_t* offsets,
+                                   const int64_t* numels, const char* sha256_hex,
+                                   char* path_out, size_t path_cap);
+ADAMW_API int ckpt_manifest_load(const char* step_dir, int32_t expected_world,
+                                 int32_t verify_sha256, int32_t* step_out,
+                                 int32_t* world_out, int64_t* offsets_out,
+                                 int64_t* numels_out, int32_t cap);
+ADAMW_API int ckpt_shard_read(adamw_ctx* ctx, const char* step_dir, int32_t rank,
+                              int32_t expected_world, int32_t* step_out, float* d_w,
+                              float* d_m, float* d_v, void* stream);
+
+/* SHA-256 (FIPS 180-4) of `bytes` bytes as 64 lowercase hex digits + NUL. */
+ADAMW_API int ckpt_sha256_hex(const void* data, int64_t bytes, char* hex_out);
+
 /* Name of a status code, and the last failure's explanation (this thread). */
 ADAMW_API const char* adamw_strerror(int status);
 ADAMW_API const char* adamw_last_error(void);

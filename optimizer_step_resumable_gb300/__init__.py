@@ -65,6 +65,17 @@ SIGNATURES = {
                                    _c.c_char_p, _c.c_size_t]),
     "ckpt_probe": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.POINTER(_c.c_int32),
                               _c.POINTER(_c.c_int32)]),
+    "ckpt_shard_write": (_c.c_int, [_vp, _c.c_char_p, _c.c_int32, _c.c_char_p]),
+    "ckpt_shard_write_host": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_int32, _c.c_int32, _vp,
+                                         _vp, _vp, _c.c_char_p]),
+    "ckpt_manifest_commit": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_int32, _c.c_double, _vp,
+                                        _vp, _c.c_char_p, _c.c_char_p, _c.c_size_t]),
+    "ckpt_manifest_load": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_int32,
+                                      _c.POINTER(_c.c_int32), _c.POINTER(_c.c_int32), _vp, _vp,
+                                      _c.c_int32]),
+    "ckpt_shard_read": (_c.c_int, [_vp, _c.c_char_p, _c.c_int32, _c.c_int32,
+                                   _c.POINTER(_c.c_int32), _vp, _vp, _vp, _vp]),
+    "ckpt_sha256_hex": (_c.c_int, [_vp, _c.c_int64, _c.c_char_p]),
     "adamw_strerror": (_c.c_char_p, [_c.c_int]),
     "adamw_last_error": (_c.c_char_p, []),
 }
@@ -378,6 +389,71 @@ def ckpt_probe(path: str, n_expected: int = -1):
                               ctypes.byref(n))
     _check(st, "ckpt_probe")
     return step.value, n.value
+
+
+def ckpt_sha256_hex(data: bytes) -> str:
+    buf = ctypes.create_string_buffer(65)
+    st = library().ckpt_sha256_hex(ctypes.c_char_p(data), len(data), buf)
+    _check(st, "ckpt_sha256_hex")
+    return buf.value.decode()
+
+
+def ckpt_shard_write(ctx: Context, directory: str, rank: int) -> str:
+    """Writes the last packed image as rank<rank>.bin; returns its sha256."""
+    buf = ctypes.create_string_buffer(65)
+    _check(library().ckpt_shard_write(ctx.handle, os.fsencode(directory), int(rank), buf),
+           "ckpt_shard_write")
+    return buf.value.decode()
+
+
+def ckpt_shard_write_host(directory: str, step: int, rank: int, w, m, v) -> str:
+    import numpy as np
+    arrs = [np.ascontiguousarray(a, dtype=np.float32) for a in (w, m, v)]
+    n = arrs[0].size
+    buf = ctypes.create_string_buffer(65)
+    st = library().ckpt_shard_write_host(os.fsencode(directory), int(step), int(rank), int(n),
+                                         *[a.ctypes.data for a in arrs], buf)
+    _check(st, "ckpt_shard_write_host")
+    return buf.value.decode()
+
+
+def ckpt_manifest_commit(directory: str, step: int, offsets, numels, digests,
+                         wall_clock_seconds: float = 0.0) -> str:
+    world = len(offsets)
+    po = (ctypes.c_int64 * world)(*offsets)
+    pn = (ctypes.c_int64 * world)(*numels)
+    buf = ctypes.create_string_buffer(4200)
+    st = library().ckpt_manifest_commit(os.fsencode(directory), int(step), world,
+                                        float(wall_clock_seconds), ctypes.addressof(po),
+                                        ctypes.addressof(pn), "".join(digests).encode(), buf,
+                                        len(buf))
+    _check(st, "ckpt_manifest_commit")
+    return buf.value.decode()
+
+
+def ckpt_manifest_load(step_dir: str, expected_world: int = -1, verify: bool = True):
+    """(step, offsets, numels) of a validated sharded checkpoint."""
+    cap = 4096
+    po = (ctypes.c_int64 * cap)()
+    pn = (ctypes.c_int64 * cap)()
+    step, world = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    st = library().ckpt_manifest_load(os.fsencode(step_dir), int(expected_world),
+                                      1 if verify else 0, ctypes.byref(step),
+                                      ctypes.byref(world), ctypes.addressof(po),
+                                      ctypes.addressof(pn), cap)
+    _check(st, "ckpt_manifest_load")
+    return step.value, list(po[:world.value]), list(pn[:world.value])
+
+
+def ckpt_shard_read(ctx: Context, step_dir: str, rank: int, w, m, v, expected_world: int = -1,
+                    stream=None) -> int:
+    n = ctx.n
+    step = ctypes.c_int32(-1)
+    st = library().ckpt_shard_read(ctx.handle, os.fsencode(step_dir), int(rank),
+                                   int(expected_world), ctypes.byref(step), _dev_ptr(w, n, "w"),
+                                   _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), _stream(stream))
+    _check(st, "ckpt_shard_read")
+    return step.value
 
 
 def adamw_strerror(status: int) -> str:

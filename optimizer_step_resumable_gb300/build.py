@@ -25,7 +25,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
              "-I" + INCLUDE]
 
 CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu", "writer.cu", "noalloc.cu"]
-CXX_SOURCES = ["ckpt_io.cpp"]
+CXX_SOURCES = ["ckpt_io.cpp", "manifest.cpp", "sha256.cpp"]
 
 
 def nvcc() -> str:

@@ -117,11 +117,20 @@ int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
 {
     if (!dir || step < 0)
         return fail(ADAMW_EINVAL, "ckpt write: null directory or negative step");
+    char name[32];
+    std::snprintf(name, sizeof name, "step_%06d.bin", int(step));
+    return write_named_file(dir, name, pieces, npieces, flags, path_out, path_cap);
+}
+
+int write_named_file(const char* dir, const char* name, const IoPiece* pieces, int npieces,
+                     int32_t flags, char* path_out, size_t path_cap)
+{
+    if (!dir || !name)
+        return fail(ADAMW_EINVAL, "ckpt write: null directory or name");
     if (!little_endian_host())
         return fail(ADAMW_EINVAL, "ckpt write: big-endian host not supported");
     char final_path[4096], tmp_path[4112];
-    const int len = std::snprintf(final_path, sizeof final_path, "%s/step_%06d.bin",
-                                  dir, int(step));
+    const int len = std::snprintf(final_path, sizeof final_path, "%s/%s", dir, name);
     if (len < 0 || size_t(len) >= sizeof final_path)
         return fail(ADAMW_EINVAL, "ckpt write: directory name too long");
     std::snprintf(tmp_path, sizeof tmp_path, "%s.tmp", final_path);

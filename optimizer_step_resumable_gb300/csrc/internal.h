@@ -4,6 +4,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <string>
+#include <vector>
 
 #include "adamw_ckpt.h"
 
@@ -96,8 +98,35 @@ struct IoPiece {
 // goes to the disk with O_DIRECT (whole blocks, then ftruncate to size).
 int write_file_atomic(const char* dir, int32_t step, const IoPiece* pieces,
                       int npieces, char* path_out, size_t path_cap, int32_t flags = 0);
+// The same for any file name in dir (used for the shard files).
+int write_named_file(const char* dir, const char* name, const IoPiece* pieces, int npieces,
+                     int32_t flags, char* path_out = nullptr, size_t path_cap = 0);
 // Deletes all but the `keep` newest step_<digits>.bin files of dir.
 int rotate_files(const char* dir, int32_t keep, int32_t* removed);
+
+// SHA-256 (FIPS 180-4), incremental (sha256.cpp).
+class Sha256 {
+public:
+    Sha256() { reset(); }
+    void reset();
+    void update(const void* data, size_t bytes);
+    void final_hex(char out[65]);  // 64 lowercase hex digits + NUL
+
+private:
+    uint32_t h_[8];
+    uint64_t len_;
+    unsigned char buf_[64];
+    size_t fill_;
+};
+
+// Sharded checkpoint (manifest.cpp).
+// Creates (if needed) <dir>/step_NNNNNN.tmp, where the ranks write their files.
+int shard_staging_dir(const char* dir, int32_t step, std::string* out);
+// Parses and checks <step_dir>/manifest.json against expected_world (< 0:
+// any) and every listed shard file (size, header, sha256 if verify).
+int load_manifest(const char* step_dir, int32_t expected_world, bool verify, int32_t* step_out,
+                  std::vector<int64_t>* offsets, std::vector<int64_t>* numels,
+                  std::vector<std::string>* paths, std::vector<std::string>* digests);
 // Validates header and size; on success *fd_out is an open descriptor
 // positioned after the header (caller closes it).
 int open_validated(const char* path, int32_t n_expected, int32_t* step_out,

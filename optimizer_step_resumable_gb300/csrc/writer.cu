@@ -13,10 +13,13 @@
 // One write is in flight at most: the pinned host image is single-buffered,
 // so the next pack (which copies into it) waits on the host for the writer.
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include <cuda_runtime.h>
+#include <unistd.h>
 
 #include "context.h"
 #include "internal.h"
@@ -194,6 +197,111 @@ int ckpt_step_end(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d
     if (rc == ADAMW_OK && action_out)
         *action_out = CKPT_ACTION_WRITING;
     return rc;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Sharded checkpoint, GPU side ("Checkpoint and Sharded Resume", lesson 80):
+// this context holds one rank's shard of the flat state.
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int ckpt_shard_write(adamw_ctx* ctx, const char* dir, int32_t rank, char* sha256_hex_out)
+{
+    osr::clear_error();
+    if (!ctx || !dir || rank < 0 || !sha256_hex_out)
+        return osr::fail(ADAMW_EINVAL, "ckpt_shard_write: bad arguments");
+    if (!ctx->packed)
+        return osr::fail(ADAMW_ESTATE, "no packed checkpoint: call ckpt_pack first");
+    osr::writer_drain(ctx);
+    {
+        const cudaError_t e = cudaEventSynchronize(ctx->ev_d2h);
+        if (e != cudaSuccess)
+            return osr::fail(ADAMW_ECUDA, "waiting for the checkpoint copy: %s",
+                             cudaGetErrorString(e));
+    }
+    ctx->d2h_pending = false;
+    std::string staging;
+    int rc = osr::shard_staging_dir(dir, ctx->packed_step, &staging);
+    if (rc != ADAMW_OK)
+        return rc;
+    char name[64];
+    std::snprintf(name, sizeof name, "rank%d.bin", int(rank));
+    const osr::IoPiece piece{ctx->h_image(), ctx->image_bytes(), ctx->h_image_capacity()};
+    rc = osr::write_named_file(staging.c_str(), name, &piece, 1, ctx->write_flags);
+    if (rc != ADAMW_OK)
+        return rc;
+    osr::Sha256 h;
+    h.update(ctx->h_image(), ctx->image_bytes());
+    h.final_hex(sha256_hex_out);
+    return ADAMW_OK;
+}
+
+int ckpt_shard_read(adamw_ctx* ctx, const char* step_dir, int32_t rank, int32_t expected_world,
+                    int32_t* step_out, float* d_w, float* d_m, float* d_v, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !step_dir || rank < 0 || !d_w || !d_m || !d_v)
+        return osr::fail(ADAMW_EINVAL, "ckpt_shard_read: bad arguments");
+    if (!ctx->has_ckpt)
+        return osr::fail(ADAMW_ESTATE, "context was created without checkpoint staging");
+    std::vector<int64_t> off, num;
+    std::vector<std::string> paths, digests;
+    int32_t step = -1;
+    // manifest and every shard's size and header; this rank's digest below
+    int rc = osr::load_manifest(step_dir, expected_world, false, &step, &off, &num, &paths,
+                                &digests);
+    if (rc != ADAMW_OK)
+        return rc;
+    if (rank >= int32_t(off.size()))
+        return osr::fail(ADAMW_EMISMATCH, "rank %d of a %zu-shard checkpoint", rank, off.size());
+    if (num[size_t(rank)] != ctx->n)
+        return osr::fail(ADAMW_EMISMATCH, "shard %d holds %lld parameters, context has %lld",
+                         rank, (long long)num[size_t(rank)], (long long)ctx->n);
+    osr::writer_drain(ctx);
+    if (ctx->d2h_pending) {
+        const cudaError_t e = cudaEventSynchronize(ctx->ev_d2h);
+        if (e != cudaSuccess)
+            return osr::fail(ADAMW_ECUDA, "cudaEventSynchronize: %s", cudaGetErrorString(e));
+        ctx->d2h_pending = false;
+    }
+    const std::string path = std::string(step_dir) + "/" + paths[size_t(rank)];
+    int fd = -1;
+    int32_t fstep = -1, fn = -1;
+    rc = osr::open_validated(path.c_str(), int32_t(ctx->n), &fstep, &fn, &fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    ctx->packed = false;  // the pinned image now holds the file
+    unsigned char* img = ctx->h_image();
+    for (int i = 0; i < 4; ++i) {
+        img[i] = static_cast<unsigned char>((uint32_t(fstep) >> (8 * i)) & 0xffu);
+        img[4 + i] = static_cast<unsigned char>((uint32_t(fn) >> (8 * i)) & 0xffu);
+    }
+    const size_t bytes = size_t(ctx->n) * 4u;
+    rc = osr::read_exact(fd, img + 8, 3 * bytes, path.c_str());
+    ::close(fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    char hex[65];
+    osr::Sha256 h;
+    h.update(img, ctx->image_bytes());
+    h.final_hex(hex);
+    if (digests[size_t(rank)] != hex)
+        return osr::fail(ADAMW_EFORMAT, "%s: sha256 %s, manifest says %s (partial or corrupted "
+                         "write)", path.c_str(), hex, digests[size_t(rank)].c_str());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(d_w, img + 8, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(d_m, img + 8 + bytes, bytes, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(d_v, img + 8 + 2 * bytes, bytes, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return osr::fail(ADAMW_ECUDA, "shard upload: %s", cudaGetErrorString(e));
+    if (step_out)
+        *step_out = step;
+    return ADAMW_OK;
 }
 
 }  // extern "C"

@@ -11,7 +11,10 @@ library's kernels.
 """
 from __future__ import annotations
 
-from . import adamw_clip_step_ex, grad_sumsq
+import time
+
+from . import (adamw_clip_step_ex, ckpt_manifest_commit, ckpt_pack, ckpt_shard_read,
+               ckpt_shard_write, grad_sumsq)
 
 
 def shard_range(n: int, rank: int, world: int, align: int = 4):
@@ -61,3 +64,37 @@ def sharded_clip_step(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=1.0, zero_gra
     adamw_clip_step_ex(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=grad_scale,
                        global_sumsq=total, zero_grad=zero_grad, stream=stream)
     return total
+
+
+def _gather_objects(obj, group=None):
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return [obj]
+    out = [None] * dist.get_world_size(group)
+    dist.all_gather_object(out, obj, group=group)
+    return out
+
+
+def save_sharded(ctx, directory, step, w, m, v, rank, world, offsets, numels, group=None,
+                 main_stream=None, side_stream=None, wall_clock_seconds=None):
+    """Sharded checkpoint of this rank's shard: pack, write rank<R>.bin and
+    take its sha256; exchange the digests; rank 0 commits the manifest and
+    renames the step directory; all ranks return its path."""
+    import torch.distributed as dist
+    ckpt_pack(ctx, step, w, m, v, main_stream=main_stream, side_stream=side_stream)
+    digest = ckpt_shard_write(ctx, directory, rank)
+    digests = _gather_objects(digest, group)
+    path = None
+    if rank == 0:
+        wall = time.time() if wall_clock_seconds is None else wall_clock_seconds
+        path = ckpt_manifest_commit(directory, step, offsets, numels, digests, wall)
+    paths = _gather_objects(path, group)
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier(group)
+    return paths[0]
+
+
+def load_sharded(ctx, step_dir, rank, world, w, m, v, stream=None):
+    """Reads this rank's shard after validating the manifest against the
+    world size and the shard's sha256; returns the stored step."""
+    return ckpt_shard_read(ctx, step_dir, rank, w, m, v, expected_world=world, stream=stream)

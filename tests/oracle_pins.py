@@ -442,4 +442,89 @@ def pin_float32_resume_bit_exact(o, tmp):
     assert np.max(np.abs(w4.astype(np.float64) - w)) > 1e-4
 
 
+
+
+# --- sharded checkpoint ------------------------------------------------------
+
+def _shards(n_per, world, seed=12):
+    rng = np.random.default_rng(seed)
+    return [tuple(rng.standard_normal(n_per).astype(np.float32) for _ in range(3))
+            for _ in range(world)]
+
+
+def pin_sharded_manifest_schema(o, tmp):
+    """The oracle's manifest has the page's keys, nesting, order and types,
+    and equal 65,536-element shards start at R x 65,536 (golden example)."""
+    from oracle import sharded
+    with open(os.path.join(GOLDEN, "manifest_example.json")) as f:
+        page = json.load(f)
+    shards = _shards(65536, 4)
+    d = sharded.save_sharded(str(tmp), 1234, shards, [0, 65536, 131072, 196608], 4521)
+    with open(os.path.join(d, "manifest.json")) as f:
+        ours = json.load(f)
+    assert list(ours) == list(page)
+    assert ours["schema_version"] == page["schema_version"] == 1
+    assert (ours["world_size"], ours["step"]) == (page["world_size"], page["step"])
+    for a, b in zip(ours["shards"], page["shards"]):
+        assert list(a) == list(b)
+        for k in ("rank", "path", "param_shard_offset", "param_shard_numel"):
+            assert a[k] == b[k], k
+        assert len(a["sha256"]) == 64
+
+
+def pin_sharded_roundtrip_and_guards(o, tmp):
+    """4 shard files + manifest, reloaded byte for byte ("Ship it"); a
+    different world size, a dropped shard and a truncated or corrupted shard
+    are refused ("Three failure modes")."""
+    import shutil
+
+    from oracle import sharded
+    shards = _shards(1000, 4)
+    d = sharded.save_sharded(str(tmp), 7, shards, [0, 1000, 2000, 3000])
+    assert sorted(os.listdir(d)) == ["manifest.json", "rank0.bin", "rank1.bin", "rank2.bin",
+                                     "rank3.bin"]
+    step, got = sharded.load_sharded(d, 4)
+    assert step == 7
+    for (off, k, w, m, v), (w0, m0, v0), r in zip(got, shards, range(4)):
+        assert (off, k) == (1000 * r, 1000)
+        assert w.tobytes() == w0.tobytes() and m.tobytes() == m0.tobytes()
+        assert v.tobytes() == v0.tobytes()
+
+    def refused(kind, mutate):
+        bad = os.path.join(str(tmp), f"bad_{kind}_{len(os.listdir(str(tmp)))}")
+        shutil.copytree(d, bad)
+        world = mutate(bad)
+        try:
+            sharded.load_sharded(bad, world)
+        except sharded.ShardedCheckpointError as e:
+            assert e.kind == kind, (e.kind, kind)
+            return
+        raise AssertionError(f"{kind} not refused")
+
+    refused("world_size", lambda b: 2)
+
+    def drop_shard(b):
+        p = os.path.join(b, "manifest.json")
+        man = json.load(open(p))
+        man["shards"] = man["shards"][:3]
+        json.dump(man, open(p, "w"))
+        return 4
+    refused("shard_count", drop_shard)
+
+    def truncate(b):
+        p = os.path.join(b, "rank2.bin")
+        data = open(p, "rb").read()
+        open(p, "wb").write(data[:-12])
+        return 4
+    refused("partial_write", truncate)
+
+    def flip(b):
+        p = os.path.join(b, "rank1.bin")
+        data = bytearray(open(p, "rb").read())
+        data[100] ^= 1
+        open(p, "wb").write(bytes(data))
+        return 4
+    refused("partial_write", flip)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
