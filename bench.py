@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--sweep", action="store_true",
+                   help="per-size kernel measurements (flat 2^20..2^30, latency at 65,536); "
+                        "prints one JSON object per size instead of the bench line")
     return p.parse_args(argv)
 
 
@@ -438,8 +441,153 @@ def run_ours(args):
     return 0
 
 
+def median_ms(fn, reps, stream):
+    """Median duration of fn() over reps, CUDA events on `stream`."""
+    import torch
+    out = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        out.append(a.elapsed_time(b))
+    return statistics.median(out), min(out), max(out)
+
+
+def run_sweep(args):
+    """Kernel rates per state size (flat vectors, g ~ 1e-3 with 0.1% outliers
+    x1000) and the launch-latency case at 65,536 parameters, plain vs graph.
+    Each kernel is timed alone (median of reps, CUDA events); between reps
+    the L2 is emptied by reading a 512 MB buffer (a read leaves no dirty
+    lines whose write-back would land in the measured kernels).  The GPU
+    time of a whole step without host launch overhead comes from replaying
+    a CUDA graph of 50 captured steps."""
+    import torch
+
+    import optimizer_step_resumable_gb300 as osr
+    from optimizer_step_resumable_gb300 import build as lib_build
+    from synthetic import device as synth_dev
+    from synthetic import workloads as W
+
+    lib_build.build()
+    dev = torch.device("cuda", 0)
+    main = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    flush = torch.ones(128 << 20, device=dev)
+    rows = []
+    for log2n in range(20, 31):
+        wl = W.flat_pow2(log2n)
+        n = wl.n
+        w = torch.empty(n, device=dev)
+        g = torch.empty(n, device=dev)
+        m = torch.zeros(n, device=dev)
+        v = torch.zeros(n, device=dev)
+        synth_dev.fill_weights(w, wl.seed)
+        synth_dev.fill_grads(g, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
+        ctx = osr.adamw_create(n)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in evs:
+            e.record(main)
+        reps = 20 if n <= (1 << 27) else 8
+        norm_ms, step_ms, whole = [], [], {"pdl": [], "no_pdl": []}
+        t = 1
+        for mode in ("split", "pdl", "no_pdl"):
+            osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_PDL if mode == "no_pdl" else 0)
+            for r in range(reps + 3):
+                flush.sum()
+                if mode == "split":  # an event between the kernels: plain order
+                    osr.adamw_record_events(ctx, *evs)
+                else:
+                    osr.adamw_record_events(ctx, evs[0], None, evs[2])
+                osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+                t += 1
+                evs[2].synchronize()
+                if r < 3:
+                    continue
+                if mode == "split":
+                    norm_ms.append(evs[0].elapsed_time(evs[1]))
+                    step_ms.append(evs[1].elapsed_time(evs[2]))
+                else:
+                    whole[mode].append(evs[0].elapsed_time(evs[2]))
+        osr.adamw_set_launch_options(ctx, 0)
+
+        def pack():
+            osr.ckpt_pack(ctx, 1, w, m, v, main_stream=main, side_stream=main)
+
+        pack_ms, _, _ = median_ms(pack, max(3, reps // 2), main)
+        osr.ckpt_wait(ctx)
+        # GPU time per step without launch overhead: 50 steps in one graph
+        # (t fixed inside the graph; the kernels' work does not depend on t)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(gr, stream=cap):
+                for _ in range(50):
+                    osr.adamw_clip_step(ctx, w, g, m, v, 100, wl.lr, wl.wd, wl.clip, stream=cap)
+        gr.replay()
+        torch.cuda.synchronize()
+        graph_ms, _, _ = median_ms(gr.replay, 5, main)
+        graph_step_ms = graph_ms / 50
+        ctx.close()
+        nm, sm = statistics.median(norm_ms), statistics.median(step_ms)
+        row = {"workload": wl.name, "n": n,
+               "k_grad_norm": {"ms": nm, "GB/s": 4 * n / nm / 1e6, "frac": 4 * n / nm / 1e6 / peak},
+               "k_clip_adamw": {"ms": sm, "GB/s": 28 * n / sm / 1e6,
+                                "frac": 28 * n / sm / 1e6 / peak},
+               "step": {"ms": nm + sm, "params/s": n / ((nm + sm) / 1e3),
+                        "GB/s": 32 * n / (nm + sm) / 1e6},
+               "step_whole": {m: {"ms": statistics.median(x),
+                                  "GB/s": 32 * n / statistics.median(x) / 1e6}
+                              for m, x in whole.items()},
+               "step_graph": {"ms": graph_step_ms, "params/s": n / (graph_step_ms / 1e3),
+                              "GB/s": 32 * n / graph_step_ms / 1e6},
+               "pack+d2h": {"ms": pack_ms, "GB/s(device 24n)": 24 * n / pack_ms / 1e6},
+               "peak_GB/s": peak, "peak_kind": peak_kind}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del w, g, m, v
+        torch.cuda.empty_cache()
+
+    # latency case: 65,536 parameters (L2-resident), plain launches vs graph
+    wl = W.flat_65k()
+    n = wl.n
+    w = torch.empty(n, device=dev)
+    g = torch.empty(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    synth_dev.fill_weights(w, wl.seed)
+    synth_dev.fill_grads(g, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
+    steps = 1000
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_graph_create(ctx, w, g, m, v)
+        out = {}
+        for mode in ("plain", "graph"):
+            for t in range(1, 50):
+                (osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip) if mode == "plain"
+                 else osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip))
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for t in range(50, 50 + steps):
+                if mode == "plain":
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+                else:
+                    osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip)
+            b.record(main)
+            b.synchronize()
+            out[mode] = {"us_per_step": 1e3 * a.elapsed_time(b) / steps,
+                         "params/s": n * steps / (a.elapsed_time(b) / 1e3)}
+    row = {"workload": wl.name, "n": n, "latency": out}
+    print(json.dumps(row), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -66,6 +66,9 @@ extern "C" {
 /* adamw_create flags. */
 #define ADAMW_CREATE_NO_CKPT 1 /* do not allocate the checkpoint staging    */
 
+/* adamw_set_launch_options flags. */
+#define ADAMW_LAUNCH_NO_PDL 1 /* launch the fused kernel after the norm ends  */
+
 /* adamw_clip_step_ex flags. */
 #define ADAMW_ZERO_GRAD 1 /* write 0 into g after reading it                */
 
@@ -183,6 +186,24 @@ ADAMW_API int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* 
 ADAMW_API int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream);
 
 /*
+ * One step as a CUDA graph, for states small enough that launch latency
+ * dominates (e.g. 65,536 parameters: L2-resident, a few microseconds per
+ * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm
+ * kernel followed by the fused clip+AdamW kernel (same kernels, same results
+ * bit for bit as adamw_clip_step) and instantiates it; the context owns it
+ * (replaced by the next adamw_graph_create, freed by adamw_graph_destroy or
+ * adamw_destroy).  adamw_graph_step writes step t's scalars (t, lr, wd, clip;
+ * bias corrections in double on the host) into the graph's two kernel nodes
+ * and launches it on `stream` -- one launch per step.  adamw_last_norm
+ * reports its norm.  ADAMW_ESTATE if no graph was created.
+ */
+ADAMW_API int adamw_graph_create(adamw_ctx* ctx, float* d_w, const float* d_g,
+                                 float* d_m, float* d_v);
+ADAMW_API int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd,
+                               double clip, void* stream);
+ADAMW_API int adamw_graph_destroy(adamw_ctx* ctx);
+
+/*
  * Waits for the last norm reduction launched on this context (by
  * grad_global_norm or adamw_clip_step) and reports it: *norm_out (may be
  * NULL) receives the norm of the (scaled) gradient in double, *scale_out
@@ -191,6 +212,17 @@ ADAMW_API int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void
  * step, if any, was skipped), ADAMW_ESTATE if no reduction ran yet.
  */
 ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out);
+
+/*
+ * Launch options.  By default the fused kernel of adamw_clip_step(_ex) is
+ * launched as a programmatic dependent of the norm kernel (sm_90+
+ * programmatic dependent launch): it may start while the norm's last blocks
+ * finish, warms L2 with its first chunk, and waits in hardware for the norm
+ * grid to complete before reading its result; results are unchanged.
+ * ADAMW_LAUNCH_NO_PDL launches it in plain stream order instead.  (An
+ * instrumentation event between the kernels also implies plain order.)
+ */
+ADAMW_API int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags);
 
 /*
  * Instrumentation: the next adamw_clip_step on this context records the given

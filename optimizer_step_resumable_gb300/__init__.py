@@ -22,6 +22,7 @@ EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9
 CREATE_NO_CKPT = 1
 CKPT_DIRECT = 1
 ZERO_GRAD = 1
+LAUNCH_NO_PDL = 1
 CKPT_REQ_WRITE, CKPT_REQ_EXIT = 1, 2
 CKPT_ACTION_NONE, CKPT_ACTION_WRITING, CKPT_ACTION_EXIT = 0, 1, 2
 
@@ -43,7 +44,12 @@ SIGNATURES = {
                                       _c.c_double, _c.c_double, _c.c_double, _c.c_double,
                                       _c.c_int32, _vp]),
     "grad_sumsq": (_c.c_int, [_vp, _vp, _c.POINTER(_c.c_double), _vp]),
+    "adamw_graph_create": (_c.c_int, [_vp, _vp, _vp, _vp, _vp]),
+    "adamw_graph_step": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
+                                    _vp]),
+    "adamw_graph_destroy": (_c.c_int, [_vp]),
     "adamw_record_events": (_c.c_int, [_vp, _vp, _vp, _vp]),
+    "adamw_set_launch_options": (_c.c_int, [_vp, _c.c_int32]),
     "adamw_clip_step_noalloc": (_c.c_int, [_vp, _vp, _vp, _vp, _c.c_int64, _c.c_int32,
                                            _c.c_double, _c.c_double, _c.c_double,
                                            _c.c_double, _c.c_double, _c.c_double, _vp, _vp]),
@@ -245,6 +251,22 @@ def grad_sumsq(ctx: Context, g, stream=None) -> float:
     return out.value
 
 
+def adamw_graph_create(ctx: Context, w, g, m, v):
+    n = ctx.n
+    _check(library().adamw_graph_create(ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"),
+                                        _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v")),
+           "adamw_graph_create")
+
+
+def adamw_graph_step(ctx: Context, t: int, lr: float, wd: float, clip: float, stream=None):
+    _check(library().adamw_graph_step(ctx.handle, int(t), float(lr), float(wd), float(clip),
+                                      _stream(stream)), "adamw_graph_step")
+
+
+def adamw_graph_destroy(ctx: Context):
+    _check(library().adamw_graph_destroy(ctx.handle), "adamw_graph_destroy")
+
+
 def adamw_last_norm(ctx: Context):
     """(norm, clip factor) of the last reduction; raises NonFiniteGradient."""
     norm, scale = ctypes.c_double(), ctypes.c_float()
@@ -271,6 +293,11 @@ def adamw_clip_step_noalloc(w, g, m, v, t: int, lr: float, wd: float, clip: floa
         int(n), int(t), float(lr), float(wd), float(clip), float(beta1), float(beta2),
         float(eps), np_, _stream(stream))
     _check(st, "adamw_clip_step_noalloc")
+
+
+def adamw_set_launch_options(ctx: Context, flags: int = 0):
+    _check(library().adamw_set_launch_options(ctx.handle, int(flags)),
+           "adamw_set_launch_options")
 
 
 def adamw_record_events(ctx: Context, ev_begin=None, ev_mid=None, ev_end=None):

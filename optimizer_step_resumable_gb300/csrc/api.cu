@@ -68,6 +68,7 @@ void free_ctx(adamw_ctx* c)
     if (!c)
         return;
     osr::writer_stop(c);
+    osr::graph_release(c);
     if (c->device >= 0) {
         DeviceScope scope(c->device);
         if (c->ev_d2h && c->d2h_pending)
@@ -124,7 +125,19 @@ int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream,
                                    c->h_res_dev, stream, grad_scale);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "norm kernel launch");
-    CUDA_TRY(cudaEventRecord(c->ev_norm, static_cast<cudaStream_t>(stream)));
+    return ADAMW_OK;
+}
+
+// Marks the end of a reduction for adamw_last_norm.  Inside a stream
+// capture the record would belong to the graph, not to a launch the host
+// can wait for, so captured steps are not tracked.
+int mark_norm(adamw_ctx* c, cudaStream_t st)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(st, &cap));
+    if (cap != cudaStreamCaptureStatusNone)
+        return ADAMW_OK;
+    CUDA_TRY(cudaEventRecord(c->ev_norm, st));
     c->norm_launched = true;
     return ADAMW_OK;
 }
@@ -148,6 +161,29 @@ int read_norm(adamw_ctx* c, double* norm_out, float* scale_out)
 }
 
 }  // namespace
+
+namespace osr {
+
+StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double wd)
+{
+    // Bias-correction and decay scalars, in double on the host, rounded to
+    // float once.
+    const double bc1 = 1.0 - std::pow(c->beta1, double(t));
+    const double bc2 = 1.0 - std::pow(c->beta2, double(t));
+    StepScalars k;
+    k.beta1 = float(c->beta1);
+    k.omb1 = float(1.0 - c->beta1);
+    k.beta2 = float(c->beta2);
+    k.omb2 = float(1.0 - c->beta2);
+    k.eps = float(c->eps);
+    k.step_size = float(lr / bc1);
+    k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+    k.decay = float(1.0 - lr * wd);
+    k.scale = 1.0f;
+    return k;
+}
+
+}  // namespace osr
 
 extern "C" {
 
@@ -272,6 +308,8 @@ int grad_global_norm(adamw_ctx* ctx, const float* d_g, double* h_norm, void* str
         return rc;
     DeviceScope scope(ctx->device);
     rc = launch_norm_on(ctx, d_g, INFINITY, stream);
+    if (rc == ADAMW_OK)
+        rc = mark_norm(ctx, static_cast<cudaStream_t>(stream));
     if (rc != ADAMW_OK || !h_norm)
         return rc;
     return read_norm(ctx, h_norm, nullptr);
@@ -307,20 +345,7 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
         return fail(ADAMW_EINVAL, "unknown flags 0x%x", flags);
     const bool external = !(global_sumsq < 0.0);  // NaN counts as given (non-finite)
 
-    // Bias-correction and decay scalars, in double on the host, rounded to
-    // float once.
-    const double bc1 = 1.0 - std::pow(ctx->beta1, double(t));
-    const double bc2 = 1.0 - std::pow(ctx->beta2, double(t));
-    osr::StepScalars k;
-    k.beta1 = float(ctx->beta1);
-    k.omb1 = float(1.0 - ctx->beta1);
-    k.beta2 = float(ctx->beta2);
-    k.omb2 = float(1.0 - ctx->beta2);
-    k.eps = float(ctx->eps);
-    k.step_size = float(lr / bc1);
-    k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
-    k.decay = float(1.0 - lr * wd);
-    k.scale = 1.0f;
+    osr::StepScalars k = osr::make_step_scalars(ctx, t, lr, wd);
     if (external) {
         // the global norm of the sharded gradient, from the ranks' sums
         const double norm = grad_scale * std::sqrt(global_sumsq);
@@ -343,12 +368,29 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
     }
     if (prof[1])
         CUDA_TRY(cudaEventRecord(prof[1], st));
+    // programmatic launch only straight behind the norm kernel (no event
+    // recorded in between)
+    const bool programmatic = !external && !prof[1] && ctx->pdl;
     const int e = osr::launch_adamw(d_w, d_g, d_m, d_v, ctx->n, k, external ? nullptr : ctx->d_res,
-                                    ctx->caps, stream, (flags & ADAMW_ZERO_GRAD) != 0);
+                                    ctx->caps, stream, (flags & ADAMW_ZERO_GRAD) != 0,
+                                    programmatic);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "clip+AdamW kernel launch");
     if (prof[2])
         CUDA_TRY(cudaEventRecord(prof[2], st));
+    if (!external)  // the norm result is complete once the step is
+        return mark_norm(ctx, st);
+    return ADAMW_OK;
+}
+
+int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    if (flags & ~ADAMW_LAUNCH_NO_PDL)
+        return fail(ADAMW_EINVAL, "unknown launch flags 0x%x", flags);
+    ctx->pdl = !(flags & ADAMW_LAUNCH_NO_PDL);
     return ADAMW_OK;
 }
 
@@ -362,6 +404,8 @@ int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream)
         return rc;
     DeviceScope scope(ctx->device);
     rc = launch_norm_on(ctx, d_g, INFINITY, stream);
+    if (rc == ADAMW_OK)
+        rc = mark_norm(ctx, static_cast<cudaStream_t>(stream));
     if (rc != ADAMW_OK)
         return rc;
     rc = read_norm(ctx, nullptr, nullptr);

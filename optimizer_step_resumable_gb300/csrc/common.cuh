@@ -43,11 +43,15 @@ inline bool aligned16(const void* p)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-inline int resident_blocks(const void* kernel, int threads, int sm_count)
+// Resident blocks of `kernel` on the whole device; *err receives the
+// occupancy query's own status (not the runtime's last error).
+inline int resident_blocks(const void* kernel, int threads, int sm_count, cudaError_t* err)
 {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
-        per_sm < 1)
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (e != cudaSuccess && *err == cudaSuccess)
+        *err = e;
+    if (e != cudaSuccess || per_sm < 1)
         per_sm = 1;
     return per_sm * sm_count;
 }

@@ -51,6 +51,7 @@ struct adamw_ctx {
     cudaEvent_t ev_norm = nullptr;
     bool norm_launched = false;
     cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
+    bool pdl = true;  // launch the fused kernel as a programmatic dependent
 
     // Checkpoint staging.  Device image at alloc + 8, so that its w region
     // (image + 8) starts on a 16-byte boundary for the pack kernel's vector
@@ -63,6 +64,15 @@ struct adamw_ctx {
     cudaEvent_t ev_pack = nullptr, ev_d2h = nullptr;
     bool packed = false, d2h_pending = false;
     int32_t packed_step = -1;
+
+    // A CUDA graph of one step (graph.cu): norm node -> fused-kernel node.
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    cudaGraphNode_t graph_norm = nullptr, graph_step = nullptr;
+    float* graph_w = nullptr;
+    const float* graph_g = nullptr;
+    float* graph_m = nullptr;
+    float* graph_v = nullptr;
 
     // Checkpoint writing: options and the writer thread.
     int32_t keep = 0;                   // rotation: newest files kept (0 = all)
@@ -82,4 +92,9 @@ namespace osr {
 void writer_drain(adamw_ctx* c);
 // Lets the writer finish its queued job, then joins the thread.
 void writer_stop(adamw_ctx* c);
+// Per-step scalars (bias corrections, step size, decay) from the context's
+// betas and eps, computed in double and rounded to float once (api.cu).
+StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double wd);
+// Frees the context's step graph, if any (graph.cu).
+void graph_release(adamw_ctx* c);
 }  // namespace osr

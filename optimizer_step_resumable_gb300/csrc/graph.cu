@@ -1,0 +1,161 @@
+// graph.cu -- one optimizer step as a CUDA graph (norm kernel node, then the
+// fused clip+AdamW node) for states small enough that launch latency
+// dominates.  The per-step scalars (bias corrections depend on t) are kernel
+// arguments, so each step rewrites the two nodes' parameters in the
+// instantiated graph (cudaGraphExecKernelNodeSetParams, which leaves launches
+// already in flight untouched) and launches it once.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "context.h"
+#include "internal.h"
+
+namespace osr {
+
+void graph_release(adamw_ctx* c)
+{
+    if (c->graph_exec)
+        cudaGraphExecDestroy(c->graph_exec);
+    if (c->graph)
+        cudaGraphDestroy(c->graph);
+    c->graph_exec = nullptr;
+    c->graph = nullptr;
+    c->graph_norm = c->graph_step = nullptr;
+    c->graph_w = c->graph_m = c->graph_v = nullptr;
+    c->graph_g = nullptr;
+}
+
+namespace {
+
+void fill_args(const adamw_ctx* c, double clip, const StepScalars& k, NormNodeArgs* na,
+               AdamwNodeArgs* aa, cudaKernelNodeParams* np, cudaKernelNodeParams* ap)
+{
+    na->g = c->graph_g;
+    na->n = c->n;
+    na->clip = clip;
+    na->grad_scale = 1.0;
+    na->partials = c->d_partials;
+    na->counter = c->d_counter;
+    na->d_res = c->d_res;
+    na->h_res = c->h_res_dev;
+    norm_node_params(na, np);
+    aa->w = c->graph_w;
+    aa->g = c->graph_g;
+    aa->m = c->graph_m;
+    aa->v = c->graph_v;
+    aa->n = c->n;
+    aa->k = k;
+    aa->d_res = c->d_res;
+    adamw_node_params(aa, c->caps, ap);
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(ADAMW_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace osr
+
+extern "C" {
+
+int adamw_graph_create(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m, float* d_v)
+{
+    using osr::fail;
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    const void* ptrs[4] = {d_w, d_g, d_m, d_v};
+    for (const void* p : ptrs)
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 3u))
+            return fail(ADAMW_EINVAL, "adamw_graph_create: null or unaligned state pointer");
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != ctx->device)
+        cudaSetDevice(ctx->device);
+    osr::graph_release(ctx);
+    ctx->graph_w = d_w;
+    ctx->graph_g = d_g;
+    ctx->graph_m = d_m;
+    ctx->graph_v = d_v;
+    osr::NormNodeArgs na;
+    osr::AdamwNodeArgs aa;
+    cudaKernelNodeParams np{}, ap{};
+    osr::fill_args(ctx, INFINITY, osr::make_step_scalars(ctx, 1, 0.0, 0.0), &na, &aa, &np, &ap);
+    cudaError_t e;
+    int rc = ADAMW_OK;
+    if ((e = cudaGraphCreate(&ctx->graph, 0)) != cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphCreate");
+    else if ((e = cudaGraphAddKernelNode(&ctx->graph_norm, ctx->graph, nullptr, 0, &np)) !=
+             cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphAddKernelNode(norm)");
+    else if ((e = cudaGraphAddKernelNode(&ctx->graph_step, ctx->graph, &ctx->graph_norm, 1,
+                                         &ap)) != cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphAddKernelNode(step)");
+    else if ((e = cudaGraphInstantiate(&ctx->graph_exec, ctx->graph, 0)) != cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphInstantiate");
+    if (rc != ADAMW_OK)
+        osr::graph_release(ctx);
+    if (prev >= 0 && prev != ctx->device)
+        cudaSetDevice(prev);
+    return rc;
+}
+
+int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd, double clip, void* stream)
+{
+    using osr::fail;
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    if (!ctx->graph_exec)
+        return fail(ADAMW_ESTATE, "no step graph: call adamw_graph_create first");
+    if (t < 1)
+        return fail(ADAMW_EINVAL, "t=%d: the first update has t = 1", t);
+    if (!(lr >= 0.0 && std::isfinite(lr)) || !(wd >= 0.0 && std::isfinite(wd)) || !(clip > 0.0))
+        return fail(ADAMW_EINVAL, "need finite lr, wd >= 0 and clip > 0");
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != ctx->device)
+        cudaSetDevice(ctx->device);
+    osr::NormNodeArgs na;
+    osr::AdamwNodeArgs aa;
+    cudaKernelNodeParams np{}, ap{};
+    osr::fill_args(ctx, clip, osr::make_step_scalars(ctx, t, lr, wd), &na, &aa, &np, &ap);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    int rc = ADAMW_OK;
+    if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_norm, &np)) !=
+        cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(norm)");
+    else if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_step, &ap)) !=
+             cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(step)");
+    else if ((e = cudaGraphLaunch(ctx->graph_exec, s)) != cudaSuccess)
+        rc = osr::cuda_fail(e, "cudaGraphLaunch");
+    else {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaStreamIsCapturing(s, &cap);
+        if (cap == cudaStreamCaptureStatusNone) {
+            if ((e = cudaEventRecord(ctx->ev_norm, s)) != cudaSuccess)
+                rc = osr::cuda_fail(e, "cudaEventRecord");
+            else
+                ctx->norm_launched = true;
+        }
+    }
+    if (prev >= 0 && prev != ctx->device)
+        cudaSetDevice(prev);
+    return rc;
+}
+
+int adamw_graph_destroy(adamw_ctx* ctx)
+{
+    osr::clear_error();
+    if (!ctx)
+        return osr::fail(ADAMW_EINVAL, "ctx is NULL");
+    osr::graph_release(ctx);
+    return ADAMW_OK;
+}
+
+}  // extern "C"

@@ -77,10 +77,39 @@ int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 void* stream, double grad_scale = 1.0);
 int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res,
-                 const KernelCaps& caps, void* stream, bool zero_grad = false);
+                 const KernelCaps& caps, void* stream, bool zero_grad = false,
+                 bool programmatic = false);
 int launch_pack(const float* w, const float* m, const float* v, int64_t n,
                 int32_t step, unsigned char* image, const KernelCaps& caps,
                 void* stream);
+
+// Kernel-node parameters for a CUDA graph of one step (graph.cu).  The
+// argument structs own the values that kernelParams point into.
+struct NormNodeArgs {
+    const float* g;
+    int64_t n;
+    double clip, grad_scale;
+    double* partials;
+    unsigned int* counter;
+    NormResult* d_res;
+    NormResult* h_res;
+    void* ptrs[8];
+};
+struct AdamwNodeArgs {
+    float* w;
+    const float* g;
+    float* m;
+    float* v;
+    int64_t n;
+    StepScalars k;
+    const NormResult* d_res;
+    void* ptrs[7];
+};
+}  // namespace osr
+struct cudaKernelNodeParams;
+namespace osr {
+int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p);
+int adamw_node_params(AdamwNodeArgs* a, const KernelCaps& caps, cudaKernelNodeParams* p);
 
 // Host file I/O (ckpt_io.cpp).
 constexpr size_t kIoBlock = 4096;  // O_DIRECT alignment of address, length and offset

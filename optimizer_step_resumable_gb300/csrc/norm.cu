@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(kNormThreads)
 {
     constexpr int U = kNormVecPerThread;
     const int tid = threadIdx.x;
+    // Let a kernel launched after this one with programmatic serialization
+    // start now: it waits (griddepcontrol.wait) for this grid's completion
+    // before it reads anything this kernel writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t ntiles = (n + kNormTileElems - 1) / kNormTileElems;
     const int64_t nfull = n / kNormTileElems;
     double acc = 0.0;
@@ -179,6 +183,26 @@ int launch_norm(const float* g, int64_t n, double clip, double* partials,
         k_grad_norm<false><<<blocks, kNormThreads, 0, s>>>(g, n, clip, grad_scale, partials,
                                                             counter, d_res, h_res_dev);
     return int(cudaGetLastError());
+}
+
+int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p)
+{
+    a->ptrs[0] = &a->g;
+    a->ptrs[1] = &a->n;
+    a->ptrs[2] = &a->clip;
+    a->ptrs[3] = &a->grad_scale;
+    a->ptrs[4] = &a->partials;
+    a->ptrs[5] = &a->counter;
+    a->ptrs[6] = &a->d_res;
+    a->ptrs[7] = &a->h_res;
+    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true>)
+                                      : reinterpret_cast<void*>(&k_grad_norm<false>);
+    p->gridDim = dim3(unsigned(norm_blocks(a->n)));
+    p->blockDim = dim3(kNormThreads);
+    p->sharedMemBytes = 0;
+    p->kernelParams = a->ptrs;
+    p->extra = nullptr;
+    return 0;
 }
 
 }  // namespace osr

@@ -76,11 +76,12 @@ __global__ void __launch_bounds__(kPackThreads)
 
 int query_pack_caps(int sm_count, KernelCaps* caps)
 {
+    cudaError_t err = cudaSuccess;
     caps->pack_vec = detail::resident_blocks(reinterpret_cast<const void*>(&k_ckpt_pack<true>),
-                                             kPackThreads, sm_count);
+                                             kPackThreads, sm_count, &err);
     caps->pack_scalar = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_ckpt_pack<false>), kPackThreads, sm_count);
-    return int(cudaGetLastError());
+        reinterpret_cast<const void*>(&k_ckpt_pack<false>), kPackThreads, sm_count, &err);
+    return int(err);
 }
 
 int launch_pack(const float* w, const float* m, const float* v, int64_t n,

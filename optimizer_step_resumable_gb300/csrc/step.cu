@@ -67,6 +67,25 @@ __global__ void __launch_bounds__(kStepThreads)
                  float* __restrict__ m, float* __restrict__ v, int64_t n,
                  StepScalars k, const NormResult* __restrict__ res)
 {
+    // When launched right behind the norm kernel with programmatic
+    // serialization, this grid may start while that kernel still runs: warm
+    // L2 with this block's first chunk (inputs the norm kernel does not
+    // write), then wait for the norm grid to finish before reading its
+    // result.  Launched normally, the wait returns at once.
+    if (kVec && res) {
+        const int64_t i0 = int64_t(blockIdx.x) * kStepThreads * kStepVec + threadIdx.x;
+        if ((i0 + (kStepVec - 1) * kStepThreads) < (n >> 2)) {
+#pragma unroll
+            for (int j = 0; j < kStepVec; ++j) {
+                const int64_t e = (i0 + j * kStepThreads) << 2;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(w + e));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(g + e));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(m + e));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(v + e));
+            }
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float s = k.scale;
     if (res) {
         if (res->nonfinite)
@@ -149,16 +168,42 @@ __global__ void __launch_bounds__(kStepThreads)
 int query_step_caps(int sm_count, KernelCaps* caps)
 {
     // the zeroing variants have the same shape; their counts are not needed
+    cudaError_t err = cudaSuccess;
     caps->step_vec = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<true, false>), kStepThreads, sm_count);
+        reinterpret_cast<const void*>(&k_clip_adamw<true, false>), kStepThreads, sm_count, &err);
     caps->step_scalar = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<false, false>), kStepThreads, sm_count);
-    return int(cudaGetLastError());
+        reinterpret_cast<const void*>(&k_clip_adamw<false, false>), kStepThreads, sm_count, &err);
+    return int(err);
 }
+
+namespace {
+
+// Launches the fused kernel; with `programmatic`, as a programmatic
+// dependent of the kernel before it in the stream (that kernel must be the
+// norm reduction, whose blocks release it early).
+template <typename Kernel>
+void launch_step(Kernel kernel, int blocks, cudaStream_t s, bool programmatic, float* w,
+                 const float* g, float* m, float* v, int64_t n, const StepScalars& k,
+                 const NormResult* d_res)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kStepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, kernel, w, g, m, v, n, k, d_res);  // status: cudaGetLastError
+}
+
+}  // namespace
 
 int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res, const KernelCaps& caps,
-                 void* stream, bool zero_grad)
+                 void* stream, bool zero_grad, bool programmatic)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool vec = detail::aligned16(w) && detail::aligned16(g) && detail::aligned16(m) &&
@@ -168,19 +213,52 @@ int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
         const int64_t want = detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
         if (zero_grad)
-            k_clip_adamw<true, true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+            launch_step(&k_clip_adamw<true, true>, blocks, s, programmatic, w, g, m, v, n, k, d_res);
         else
-            k_clip_adamw<true, false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+            launch_step(&k_clip_adamw<true, false>, blocks, s, programmatic, w, g, m, v, n, k,
+                        d_res);
     } else {
         const int cap = caps.step_scalar;
         const int64_t want = detail::ceil_div(n, kStepThreads);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
         if (zero_grad)
-            k_clip_adamw<false, true><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+            launch_step(&k_clip_adamw<false, true>, blocks, s, programmatic, w, g, m, v, n, k,
+                        d_res);
         else
-            k_clip_adamw<false, false><<<blocks, kStepThreads, 0, s>>>(w, g, m, v, n, k, d_res);
+            launch_step(&k_clip_adamw<false, false>, blocks, s, programmatic, w, g, m, v, n, k,
+                        d_res);
     }
     return int(cudaGetLastError());
+}
+
+int adamw_node_params(AdamwNodeArgs* a, const KernelCaps& caps, cudaKernelNodeParams* p)
+{
+    a->ptrs[0] = &a->w;
+    a->ptrs[1] = &a->g;
+    a->ptrs[2] = &a->m;
+    a->ptrs[3] = &a->v;
+    a->ptrs[4] = &a->n;
+    a->ptrs[5] = &a->k;
+    a->ptrs[6] = &a->d_res;
+    const bool vec = detail::aligned16(a->w) && detail::aligned16(a->g) &&
+                     detail::aligned16(a->m) && detail::aligned16(a->v);
+    int64_t want;
+    int cap;
+    if (vec) {
+        p->func = reinterpret_cast<void*>(&k_clip_adamw<true, false>);
+        want = detail::ceil_div(a->n >> 2, int64_t(kStepThreads) * kStepVec);
+        cap = caps.step_vec;
+    } else {
+        p->func = reinterpret_cast<void*>(&k_clip_adamw<false, false>);
+        want = detail::ceil_div(a->n, kStepThreads);
+        cap = caps.step_scalar;
+    }
+    p->gridDim = dim3(unsigned(want < 1 ? 1 : (want > cap ? cap : want)));
+    p->blockDim = dim3(kStepThreads);
+    p->sharedMemBytes = 0;
+    p->kernelParams = a->ptrs;
+    p->extra = nullptr;
+    return 0;
 }
 
 }  // namespace osr
