@@ -70,7 +70,8 @@ extern "C" {
 #define ADAMW_LAUNCH_NO_PDL 1 /* launch the fused kernel after the norm ends  */
 
 /* adamw_clip_step_ex flags. */
-#define ADAMW_ZERO_GRAD 1 /* write 0 into g after reading it                */
+#define ADAMW_ZERO_GRAD 1    /* write 0 into g after reading it             */
+#define ADAMW_TENSOR_NORMS 2 /* also sum g^2 per tensor of the offset table */
 
 /* ckpt_set_options / ckpt_write_image flags. */
 #define CKPT_DIRECT 1 /* write with O_DIRECT when the file system allows it */
@@ -159,7 +160,9 @@ ADAMW_API int adamw_clip_step(adamw_ctx* ctx, float* d_w, const float* d_g, floa
  * step, zero_grads): grad_scale > 0 multiplies the gradient before the norm,
  * the clip and the update, folded into the clip factor at no extra traffic;
  * flags ADAMW_ZERO_GRAD makes the fused kernel write 0 into d_g after reading
- * it (+4 bytes per parameter; a skipped non-finite step leaves g as is).
+ * it (+4 bytes per parameter; a skipped non-finite step leaves g as is);
+ * ADAMW_TENSOR_NORMS also computes the per-tensor sums of squares of the raw
+ * gradient (adamw_last_tensor_sumsq; not with global_sumsq >= 0).
  *
  * Sharded state (ZeRO-1 style: each rank owns one contiguous range of the
  * flat state and holds the gradient of that range): global_sumsq >= 0 is the
@@ -202,6 +205,25 @@ ADAMW_API int adamw_graph_create(adamw_ctx* ctx, float* d_w, const float* d_g,
 ADAMW_API int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd,
                                double clip, void* stream);
 ADAMW_API int adamw_graph_destroy(adamw_ctx* ctx);
+
+/*
+ * Per-tensor sums of squares ([T] "The Exact Targets of Clipping and AdamW":
+ * record the norms of all parameters to detect numerical faults): g^2 summed
+ * over each tensor of the offset table, in table order, computed by the same
+ * reduction pass as the global norm at no extra memory traffic (its blocks
+ * take contiguous tile ranges and flush a tensor's share where the next
+ * tensor starts; the host adds the shares in block order, so the values are
+ * bit-stable from run to run).
+ * grad_tensor_sumsq: reduces d_g, waits, writes n_tensors doubles to h_out;
+ * returns ADAMW_ENONFINITE (with the values stored, inf/nan in the affected
+ * tensors) if the global sum is not finite.
+ * adamw_last_tensor_sumsq: the per-tensor sums of the last step launched
+ * with ADAMW_TENSOR_NORMS (waits for it); ADAMW_ESTATE if the last reduction
+ * did not compute them.  Read them before the next step reuses the scratch.
+ */
+ADAMW_API int grad_tensor_sumsq(adamw_ctx* ctx, const float* d_g, double* h_out,
+                                void* stream);
+ADAMW_API int adamw_last_tensor_sumsq(adamw_ctx* ctx, double* h_out);
 
 /*
  * Waits for the last norm reduction launched on this context (by

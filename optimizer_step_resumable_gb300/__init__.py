@@ -22,6 +22,7 @@ EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9
 CREATE_NO_CKPT = 1
 CKPT_DIRECT = 1
 ZERO_GRAD = 1
+TENSOR_NORMS = 2
 LAUNCH_NO_PDL = 1
 CKPT_REQ_WRITE, CKPT_REQ_EXIT = 1, 2
 CKPT_ACTION_NONE, CKPT_ACTION_WRITING, CKPT_ACTION_EXIT = 0, 1, 2
@@ -44,6 +45,8 @@ SIGNATURES = {
                                       _c.c_double, _c.c_double, _c.c_double, _c.c_double,
                                       _c.c_int32, _vp]),
     "grad_sumsq": (_c.c_int, [_vp, _vp, _c.POINTER(_c.c_double), _vp]),
+    "grad_tensor_sumsq": (_c.c_int, [_vp, _vp, _vp, _vp]),
+    "adamw_last_tensor_sumsq": (_c.c_int, [_vp, _vp]),
     "adamw_graph_create": (_c.c_int, [_vp, _vp, _vp, _vp, _vp]),
     "adamw_graph_step": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
                                     _vp]),
@@ -231,15 +234,40 @@ def adamw_clip_step(ctx: Context, w, g, m, v, t: int, lr: float, wd: float,
 
 def adamw_clip_step_ex(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, clip: float,
                        grad_scale: float = 1.0, global_sumsq: float = -1.0,
-                       zero_grad: bool = False, stream=None):
+                       zero_grad: bool = False, tensor_norms: bool = False, stream=None):
     """adamw_clip_step with a gradient scale (micro-batch averaging), an
-    optional global sum of squares (sharded state) and ZERO_GRAD."""
+    optional global sum of squares (sharded state), ZERO_GRAD and
+    TENSOR_NORMS."""
     n = ctx.n
+    flags = (ZERO_GRAD if zero_grad else 0) | (TENSOR_NORMS if tensor_norms else 0)
     st = library().adamw_clip_step_ex(
         ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"), _dev_ptr(m, n, "m"),
         _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip), float(grad_scale),
-        float(global_sumsq), ZERO_GRAD if zero_grad else 0, _stream(stream))
+        float(global_sumsq), flags, _stream(stream))
     _check(st, "adamw_clip_step_ex")
+
+
+def grad_tensor_sumsq(ctx: Context, g, stream=None):
+    """Per-tensor sums of squares (numpy float64, table order); raises
+    NonFiniteGradient (with .values set) if the global sum is not finite."""
+    import numpy as np
+    out = np.empty(ctx.num_tensors, np.float64)
+    st = library().grad_tensor_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g"), out.ctypes.data,
+                                     _stream(stream))
+    if st == ENONFINITE:
+        err = NonFiniteGradient(st, "grad_tensor_sumsq", adamw_last_error())
+        err.values = out
+        raise err
+    _check(st, "grad_tensor_sumsq")
+    return out
+
+
+def adamw_last_tensor_sumsq(ctx: Context):
+    import numpy as np
+    out = np.empty(ctx.num_tensors, np.float64)
+    _check(library().adamw_last_tensor_sumsq(ctx.handle, out.ctypes.data),
+           "adamw_last_tensor_sumsq")
+    return out
 
 
 def grad_sumsq(ctx: Context, g, stream=None) -> float:

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI entry points of include/adamw_ckpt.h: the context that
 // owns all scratch, the host-side scalars, the launch sequence of one step,
 // and the checkpoint pack / write / read around the staging images.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -79,6 +80,11 @@ void free_ctx(adamw_ctx* c)
         if (c->ev_pack) cudaEventDestroy(c->ev_pack);
         if (c->ev_d2h) cudaEventDestroy(c->ev_d2h);
         if (c->d_scratch) cudaFree(c->d_scratch);
+        if (c->d_tab_offsets) cudaFree(c->d_tab_offsets);
+        if (c->d_kfirst) cudaFree(c->d_kfirst);
+        if (c->d_segbase) cudaFree(c->d_segbase);
+        if (c->d_seg_sums) cudaFree(c->d_seg_sums);
+        if (c->h_seg_sums) cudaFreeHost(c->h_seg_sums);
         if (c->h_res) cudaFreeHost(c->h_res);
         if (c->d_image_alloc) cudaFree(c->d_image_alloc);
         if (c->h_image_alloc) cudaFreeHost(c->h_image_alloc);
@@ -119,12 +125,34 @@ int validate_table(int64_t n, const int64_t* offsets, const int64_t* numels, int
 }
 
 int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream,
-                   double grad_scale = 1.0)
+                   double grad_scale = 1.0, bool tensor_sums = false)
 {
+    const osr::TensorSegs segs{c->d_tab_offsets, c->d_kfirst, c->d_segbase, c->d_seg_sums};
     const int e = osr::launch_norm(g, c->n, clip, c->d_partials, c->d_counter, c->d_res,
-                                   c->h_res_dev, stream, grad_scale);
+                                   c->h_res_dev, stream, grad_scale,
+                                   tensor_sums ? &segs : nullptr);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "norm kernel launch");
+    c->segs_launched = tensor_sums;
+    return ADAMW_OK;
+}
+
+// Per-tensor sums from the segment slots of the last reduction, added in
+// block order (deterministic).  Waits for that reduction.
+int read_tensor_sums(adamw_ctx* c, double* out)
+{
+    if (!c->norm_launched || !c->segs_launched)
+        return fail(ADAMW_ESTATE, "the last reduction did not compute per-tensor sums");
+    CUDA_TRY(cudaEventSynchronize(c->ev_norm));
+    CUDA_TRY(cudaMemcpy(c->h_seg_sums, c->d_seg_sums, sizeof(double) * size_t(c->nseg),
+                        cudaMemcpyDeviceToHost));
+    const size_t nt = c->offsets.size();
+    for (size_t k = 0; k < nt; ++k)
+        out[k] = 0.0;
+    const int blocks = int(c->kfirst.size());
+    for (int b = 0; b < blocks; ++b)
+        for (int32_t s = c->segbase[size_t(b)]; s < c->segbase[size_t(b) + 1]; ++s)
+            out[size_t(c->kfirst[size_t(b)] + (s - c->segbase[size_t(b)]))] += c->h_seg_sums[s];
     return ADAMW_OK;
 }
 
@@ -248,6 +276,46 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
     if ((e = cudaEventCreateWithFlags(&c->ev_norm, cudaEventDisableTiming)) != cudaSuccess)
         return bail(cuda_fail(e, "cudaEventCreate"));
 
+    // per-tensor sums: each norm block's range [lo, hi) touches the tensors
+    // kfirst .. klast; their slots follow the previous block's
+    {
+        const int blocks = osr::norm_blocks(n_params);
+        std::vector<int64_t> tab(c->offsets);
+        tab.push_back(n_params);
+        c->kfirst.assign(size_t(blocks), 0);
+        c->segbase.assign(size_t(blocks) + 1, 0);
+        auto tensor_of = [&](int64_t e) {  // last k with offsets[k] <= e
+            return int32_t(std::upper_bound(tab.begin(), tab.end() - 1, e) - tab.begin() - 1);
+        };
+        for (int b = 0; b < blocks; ++b) {
+            const int64_t lo = osr::norm_block_tile(n_params, b) * osr::kNormTileElems;
+            int64_t hi = osr::norm_block_tile(n_params, b + 1) * osr::kNormTileElems;
+            if (hi > n_params)
+                hi = n_params;
+            c->kfirst[size_t(b)] = tensor_of(lo);
+            c->segbase[size_t(b) + 1] =
+                c->segbase[size_t(b)] + (tensor_of(hi - 1) - c->kfirst[size_t(b)] + 1);
+        }
+        c->nseg = c->segbase[size_t(blocks)];
+        if ((e = cudaMalloc(&c->d_tab_offsets, sizeof(int64_t) * tab.size())) != cudaSuccess ||
+            (e = cudaMalloc(&c->d_kfirst, sizeof(int32_t) * size_t(blocks))) != cudaSuccess ||
+            (e = cudaMalloc(&c->d_segbase, sizeof(int32_t) * (size_t(blocks) + 1))) !=
+                cudaSuccess ||
+            (e = cudaMalloc(&c->d_seg_sums, sizeof(double) * size_t(c->nseg))) != cudaSuccess ||
+            (e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_seg_sums),
+                               sizeof(double) * size_t(c->nseg), cudaHostAllocDefault)) !=
+                cudaSuccess)
+            return bail(cuda_fail(e, "allocating the per-tensor scratch"));
+        if ((e = cudaMemcpy(c->d_tab_offsets, tab.data(), sizeof(int64_t) * tab.size(),
+                            cudaMemcpyHostToDevice)) != cudaSuccess ||
+            (e = cudaMemcpy(c->d_kfirst, c->kfirst.data(), sizeof(int32_t) * size_t(blocks),
+                            cudaMemcpyHostToDevice)) != cudaSuccess ||
+            (e = cudaMemcpy(c->d_segbase, c->segbase.data(),
+                            sizeof(int32_t) * (size_t(blocks) + 1), cudaMemcpyHostToDevice)) !=
+                cudaSuccess)
+            return bail(cuda_fail(e, "uploading the offset table"));
+    }
+
     if (!(flags & ADAMW_CREATE_NO_CKPT)) {
         const size_t bytes = 16 + size_t(12) * size_t(n_params);
         if ((e = cudaMalloc(&c->d_image_alloc, bytes)) != cudaSuccess) {
@@ -341,7 +409,7 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
         return fail(ADAMW_EINVAL, "clip=%g must be > 0 (INFINITY disables clipping)", clip);
     if (!(grad_scale > 0.0 && std::isfinite(grad_scale)))
         return fail(ADAMW_EINVAL, "grad_scale=%g must be finite and > 0", grad_scale);
-    if (flags & ~ADAMW_ZERO_GRAD)
+    if (flags & ~(ADAMW_ZERO_GRAD | ADAMW_TENSOR_NORMS))
         return fail(ADAMW_EINVAL, "unknown flags 0x%x", flags);
     const bool external = !(global_sumsq < 0.0);  // NaN counts as given (non-finite)
 
@@ -362,7 +430,8 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
     if (prof[0])
         CUDA_TRY(cudaEventRecord(prof[0], st));
     if (!external) {
-        rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale);
+        rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale,
+                            (flags & ADAMW_TENSOR_NORMS) != 0);
         if (rc != ADAMW_OK)
             return rc;
     }
@@ -381,6 +450,35 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
     if (!external)  // the norm result is complete once the step is
         return mark_norm(ctx, st);
     return ADAMW_OK;
+}
+
+int grad_tensor_sumsq(adamw_ctx* ctx, const float* d_g, double* h_out, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !h_out)
+        return fail(ADAMW_EINVAL, "ctx or h_out is NULL");
+    int rc = check_state_ptr(d_g, "d_g");
+    if (rc != ADAMW_OK)
+        return rc;
+    DeviceScope scope(ctx->device);
+    rc = launch_norm_on(ctx, d_g, INFINITY, stream, 1.0, true);
+    if (rc == ADAMW_OK)
+        rc = mark_norm(ctx, static_cast<cudaStream_t>(stream));
+    if (rc != ADAMW_OK)
+        return rc;
+    rc = read_tensor_sums(ctx, h_out);
+    if (rc != ADAMW_OK)
+        return rc;
+    return read_norm(ctx, nullptr, nullptr);
+}
+
+int adamw_last_tensor_sumsq(adamw_ctx* ctx, double* h_out)
+{
+    osr::clear_error();
+    if (!ctx || !h_out)
+        return fail(ADAMW_EINVAL, "ctx or h_out is NULL");
+    DeviceScope scope(ctx->device);
+    return read_tensor_sums(ctx, h_out);
 }
 
 int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags)

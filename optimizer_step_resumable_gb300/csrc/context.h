@@ -50,6 +50,17 @@ struct adamw_ctx {
     osr::NormResult* h_res_dev = nullptr;  // device view of the same memory
     cudaEvent_t ev_norm = nullptr;
     bool norm_launched = false;
+
+    // Per-tensor sums of squares: the table on the device, the norm grid's
+    // per-block segment layout (host and device), the segment sums.
+    int64_t* d_tab_offsets = nullptr;  // n_tensors + 1 (last = n)
+    int32_t* d_kfirst = nullptr;       // per norm block
+    int32_t* d_segbase = nullptr;      // per norm block + 1
+    double* d_seg_sums = nullptr;
+    double* h_seg_sums = nullptr;      // pinned
+    std::vector<int32_t> kfirst, segbase;
+    int32_t nseg = 0;
+    bool segs_launched = false;        // the last reduction also wrote segments
     cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
     bool pdl = true;  // launch the fused kernel as a programmatic dependent
 

@@ -70,11 +70,30 @@ struct KernelCaps {
 // Kernel launchers (norm.cu, step.cu, pack.cu).  All return cudaError_t as int.
 int query_step_caps(int sm_count, KernelCaps* caps);
 int query_pack_caps(int sm_count, KernelCaps* caps);
+// Per-tensor outputs of the norm kernel (see norm.cu).  offsets: n_tensors
+// + 1 entries (the last is n); kfirst / segbase: per block, the first tensor
+// its range touches and the index of its first segment slot; seg_sums: one
+// double per (block, tensor) pair.
+struct TensorSegs {
+    const int64_t* offsets;
+    const int32_t* kfirst;
+    const int32_t* segbase;
+    double* seg_sums;
+};
+// Block b of the norm kernel reduces the contiguous tiles
+// [ntiles b / P, ntiles (b + 1) / P) (P = norm_blocks(n)).
+inline int64_t norm_block_tile(int64_t n, int b)
+{
+    const int64_t ntiles = (n + kNormTileElems - 1) / kNormTileElems;
+    return ntiles * int64_t(b) / int64_t(norm_blocks(n));
+}
+
 // The norm kernel publishes norm = grad_scale sqrt(sum g^2) and the factor
-// applied to g: grad_scale * (norm > clip ? clip / norm : 1).
+// applied to g: grad_scale * (norm > clip ? clip / norm : 1); with segs, also
+// the per-tensor segment sums.
 int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream, double grad_scale = 1.0);
+                void* stream, double grad_scale = 1.0, const TensorSegs* segs = nullptr);
 int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res,
                  const KernelCaps& caps, void* stream, bool zero_grad = false,
@@ -93,7 +112,8 @@ struct NormNodeArgs {
     unsigned int* counter;
     NormResult* d_res;
     NormResult* h_res;
-    void* ptrs[8];
+    TensorSegs segs;
+    void* ptrs[9];
 };
 struct AdamwNodeArgs {
     float* w;

@@ -69,25 +69,56 @@ __device__ __forceinline__ double run_sumsq(const float4 (&x)[U])
     return d;
 }
 
+// This thread's share of one tile restricted to elements [lo, hi): exact
+// double squares (used only on tiles where a tensor of the offset table
+// starts, to split the tile between tensors).
+template <int U>
+__device__ __forceinline__ double thread_sumsq_in(const float4 (&x)[U], int64_t base, int tid,
+                                                  int64_t lo, int64_t hi)
+{
+    double d = 0.0;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        const int64_t e = base + (int64_t(j * kNormThreads + tid) << 2);
+        const float c[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (e + q >= lo && e + q < hi)
+                d += double(c[q]) * double(c[q]);
+    }
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // Global L2 norm, two levels in one launch.
 //
 // Level 1: the flat vector is cut into tiles of kNormTileElems elements;
-// block b takes tiles b, b + P, b + 2P, ... (P = norm_blocks(n), a function
-// of n alone).  Thread t of a tile holds U = kNormVecPerThread float4s at
-// float4 index j*256 + t (coalesced), sums their squares as one run, and
-// adds the run into a double.  The block's doubles are summed with a fixed
-// shuffle tree into partials[b].
+// block b takes the contiguous tiles [T b / P, T (b + 1) / P) (T tiles,
+// P = norm_blocks(n): a function of n alone).  Thread t of a tile holds
+// U = kNormVecPerThread float4s at float4 index j*256 + t (coalesced), sums
+// their squares as one run, and adds the run into a double.  The block's
+// doubles are summed with a fixed shuffle tree into partials[b].
 // Level 2: the block that finishes last (atomic ticket) sums partials[0..P)
 // in a fixed order -- independent of which block that is -- takes the square
 // root and the clip factor, and publishes the result.  No block waits on
 // another; the ticket counter is reset for the next launch.
+//
+// kSegs: also the sum of squares of each tensor of the offset table, at no
+// extra traffic.  Because a block's tiles are contiguous, its threads keep
+// one running sum for the tensor they are in; on a tile where a tensor
+// starts, each thread splits its elements between the tensors (exact
+// doubles) and the block writes the finished tensor's share to its next
+// segment slot (slots laid out by the host: block b's tensors are
+// kfirst[b] .. kfirst[b+1], their slots start at segbase[b]).  The host adds
+// each tensor's slots in block order.
 // ---------------------------------------------------------------------------
-template <bool kVec>
-__global__ void __launch_bounds__(kNormThreads)
+// (at least 4 resident blocks per SM, so that the fixed 608-block grid is one
+// wave on 152 SMs whichever variant runs)
+template <bool kVec, bool kSegs>
+__global__ void __launch_bounds__(kNormThreads, 4)
     k_grad_norm(const float* __restrict__ g, int64_t n, double clip, double grad_scale,
                 double* __restrict__ partials, unsigned int* __restrict__ counter,
-                NormResult* __restrict__ d_res, NormResult* h_res)
+                NormResult* __restrict__ d_res, NormResult* h_res, TensorSegs segs)
 {
     constexpr int U = kNormVecPerThread;
     const int tid = threadIdx.x;
@@ -97,8 +128,18 @@ __global__ void __launch_bounds__(kNormThreads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t ntiles = (n + kNormTileElems - 1) / kNormTileElems;
     const int64_t nfull = n / kNormTileElems;
+    const int64_t t_lo = ntiles * int64_t(blockIdx.x) / int64_t(gridDim.x);
+    const int64_t t_hi = ntiles * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
     double acc = 0.0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    double seg = 0.0;
+    int32_t k = 0, slot = 0;
+    int64_t next_start = 0;  // where tensor k + 1 starts
+    if (kSegs) {
+        k = segs.kfirst[blockIdx.x];
+        slot = segs.segbase[blockIdx.x];
+        next_start = segs.offsets[k + 1];
+    }
+    for (int64_t tile = t_lo; tile < t_hi; ++tile) {
         const int64_t base = tile * kNormTileElems;
         float4 x[U];
         if (tile < nfull) {
@@ -124,7 +165,36 @@ __global__ void __launch_bounds__(kNormThreads)
                 x[j].w = e + 3 < n ? g[e + 3] : 0.0f;
             }
         }
-        acc += run_sumsq<U>(x);
+        const double r = run_sumsq<U>(x);
+        acc += r;
+        if (kSegs) {
+            const int64_t tile_end = base + kNormTileElems < n ? base + kNormTileElems : n;
+            if (tile_end <= next_start) {
+                seg += r;  // the whole tile lies in tensor k
+            } else {
+                // block-uniform branch: every thread sees the same tile
+                int64_t lo = base;
+                for (;;) {
+                    const int64_t hi = next_start < tile_end ? next_start : tile_end;
+                    seg += thread_sumsq_in<U>(x, base, tid, lo, hi);
+                    if (next_start >= tile_end)
+                        break;
+                    const double done = block_sum<kNormThreads>(seg);
+                    if (tid == 0)
+                        segs.seg_sums[slot] = done;
+                    seg = 0.0;
+                    ++slot;
+                    ++k;
+                    lo = next_start;
+                    next_start = segs.offsets[k + 1];
+                }
+            }
+        }
+    }
+    if (kSegs) {
+        const double done = block_sum<kNormThreads>(seg);
+        if (tid == 0)
+            segs.seg_sums[slot] = done;
     }
 
     acc = block_sum<kNormThreads>(acc);
@@ -172,16 +242,28 @@ __global__ void __launch_bounds__(kNormThreads)
 
 int launch_norm(const float* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream, double grad_scale)
+                void* stream, double grad_scale, const TensorSegs* segs)
 {
     const int blocks = norm_blocks(n);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (detail::aligned16(g))
-        k_grad_norm<true><<<blocks, kNormThreads, 0, s>>>(g, n, clip, grad_scale, partials,
-                                                           counter, d_res, h_res_dev);
-    else
-        k_grad_norm<false><<<blocks, kNormThreads, 0, s>>>(g, n, clip, grad_scale, partials,
-                                                            counter, d_res, h_res_dev);
+    const TensorSegs none{nullptr, nullptr, nullptr, nullptr};
+    const TensorSegs sg = segs ? *segs : none;
+    const bool vec = detail::aligned16(g);
+    if (segs) {
+        if (vec)
+            k_grad_norm<true, true><<<blocks, kNormThreads, 0, s>>>(
+                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+        else
+            k_grad_norm<false, true><<<blocks, kNormThreads, 0, s>>>(
+                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+    } else {
+        if (vec)
+            k_grad_norm<true, false><<<blocks, kNormThreads, 0, s>>>(
+                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+        else
+            k_grad_norm<false, false><<<blocks, kNormThreads, 0, s>>>(
+                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+    }
     return int(cudaGetLastError());
 }
 
@@ -195,8 +277,10 @@ int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p)
     a->ptrs[5] = &a->counter;
     a->ptrs[6] = &a->d_res;
     a->ptrs[7] = &a->h_res;
-    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true>)
-                                      : reinterpret_cast<void*>(&k_grad_norm<false>);
+    a->segs = TensorSegs{nullptr, nullptr, nullptr, nullptr};
+    a->ptrs[8] = &a->segs;
+    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true, false>)
+                                      : reinterpret_cast<void*>(&k_grad_norm<false, false>);
     p->gridDim = dim3(unsigned(norm_blocks(a->n)));
     p->blockDim = dim3(kNormThreads);
     p->sharedMemBytes = 0;

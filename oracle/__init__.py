@@ -79,6 +79,9 @@ class Oracle:
         lib.oracle_sumsq.restype = c.c_double
         lib.oracle_global_norm.argtypes = [_f32p, c.c_int64]
         lib.oracle_global_norm.restype = c.c_double
+        lib.oracle_tensor_sumsq.argtypes = [_f32p, _i64p, _i64p, c.c_int32,
+                                             np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")]
+        lib.oracle_tensor_sumsq.restype = None
         lib.oracle_clip_scale.argtypes = [c.c_double, c.c_double]
         lib.oracle_clip_scale.restype = c.c_double
         lib.oracle_adamw_element.argtypes = [
@@ -128,6 +131,17 @@ class Oracle:
     def global_norm(self, g: np.ndarray) -> float:
         g = _f32(g)
         return self._lib.oracle_global_norm(g, g.size)
+
+    def tensor_sumsq(self, g, offsets, numels) -> np.ndarray:
+        """Sum of squares of each tensor of the offset table (double)."""
+        g = _f32(g)
+        off = np.ascontiguousarray(offsets, dtype=np.int64)
+        num = np.ascontiguousarray(numels, dtype=np.int64)
+        if off.size != num.size or (off.size and (off.min() < 0 or (off + num).max() > g.size)):
+            raise ValueError("offset table outside g")
+        out = np.empty(off.size, np.float64)
+        self._lib.oracle_tensor_sumsq(g, off, num, off.size, out)
+        return out
 
     def clip_scale(self, norm: float, clip: float) -> float:
         return self._lib.oracle_clip_scale(float(norm), float(clip))

@@ -69,6 +69,20 @@ double oracle_global_norm(const float* g, int64_t n)
 }
 
 /* ------------------------------------------------------------------------
+ * Per-tensor sums of squares.  "Training as a Recoverable State Transition"
+ * (aihero.club), section "The Exact Targets of Clipping and AdamW": the norms
+ * of all parameters are recorded to detect numerical faults.  Tensor k is
+ * g[offsets[k] .. offsets[k] + numels[k]); each sum is taken in index order
+ * in double, like the global one.
+ * ---------------------------------------------------------------------- */
+void oracle_tensor_sumsq(const float* g, const int64_t* offsets,
+                         const int64_t* numels, int32_t n_tensors, double* out)
+{
+    for (int32_t k = 0; k < n_tensors; ++k)
+        out[k] = oracle_sumsq(g + offsets[k], numels[k]);
+}
+
+/* ------------------------------------------------------------------------
  * Clip factor.  [T] "The Exact Targets of Clipping and AdamW": when the norm
  * exceeds the threshold c the whole vector is multiplied by c/||g||,
  * otherwise it is left unchanged; one c for all layers.  The worked code on

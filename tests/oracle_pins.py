@@ -205,6 +205,23 @@ def pin_norm_exact_sum(o, tmp):
         assert math.isclose(o.global_norm(g), math.sqrt(exact), rel_tol=n * 2.3e-16)
 
 
+def pin_tensor_norms(o, tmp):
+    """Per-tensor sums: Pythagorean tensors give 25, 169 and 0; the tensor
+    sums add up to the global sum exactly for small integers; a one-tensor
+    table gives the global sum."""
+    g = np.array([3, 4, 5, 12, 0, 0, 0, 1, 2, 2], np.float32)
+    got = o.tensor_sumsq(g, [0, 2, 4, 7], [2, 2, 3, 3])
+    assert list(got) == [25.0, 169.0, 0.0, 9.0]
+    assert got.sum() == o.sumsq(g)
+    rng = np.random.default_rng(13)
+    h = rng.integers(-50, 51, 1000).astype(np.float32)
+    bounds = [0, 1, 2, 10, 500, 999]
+    off = bounds
+    num = [b - a for a, b in zip(bounds, bounds[1:] + [1000])]
+    assert o.tensor_sumsq(h, off, num).sum() == o.sumsq(h)
+    assert o.tensor_sumsq(h, [0], [1000])[0] == o.sumsq(h)
+
+
 def pin_norm_homogeneous(o, tmp):
     """||2^k g|| = 2^k ||g|| exactly (power-of-two scaling is exact)."""
     g = np.random.default_rng(3).standard_normal(999).astype(np.float32)

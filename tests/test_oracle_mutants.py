@@ -61,6 +61,10 @@ MUTANTS = {
     "step_rounds_m_from_v": ("m[i] = (float)r.m;", "m[i] = (float)r.v;"),
     "step_t_off_by_one": ("double s = oracle_clip_scale(norm, clip);",
                           "double s = oracle_clip_scale(norm, clip);\n    t = t + 1;"),
+    "tensor_sum_skips_last": ("out[k] = oracle_sumsq(g + offsets[k], numels[k]);",
+                              "out[k] = oracle_sumsq(g + offsets[k], numels[k] - 1);"),
+    "tensor_sum_shifted": ("out[k] = oracle_sumsq(g + offsets[k], numels[k]);",
+                           "out[k] = oracle_sumsq(g + offsets[k] + 1, numels[k]);"),
     "scaled_clip_on_raw_norm": ("double x = (double)g[i] * grad_scale;\n        sumsq = sumsq + x * x;",
                                 "double x = (double)g[i];\n        sumsq = sumsq + x * x;"),
     "scaled_update_unscaled": ("oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,",
