@@ -550,6 +550,39 @@ def run_sweep(args):
         del w, g, m, v
         torch.cuda.empty_cache()
 
+    # mixed precision on the 110M tensor list: bfloat16 gradient, bfloat16
+    # copy of the new weights (2 + 28 bytes per parameter)
+    wl = W.gpt_110m()
+    n = wl.n
+    off, num = wl.table()
+    w = torch.empty(n, device=dev)
+    g32 = torch.empty(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    synth_dev.fill_weights(w, wl.seed)
+    synth_dev.fill_grads(g32, wl.seed, 1, wl.grad_sigma)
+    g16 = g32.to(torch.bfloat16)
+    del g32
+    w_lp = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+        times = []
+        for t in range(1, 24):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            osr.adamw_clip_step_mixed(ctx, w, g16, m, v, t, wl.lr, wl.wd, wl.clip, w_lp=w_lp)
+            b.record(main)
+            b.synchronize()
+            if t > 3:
+                times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+    row = {"workload": wl.name + " mixed (bf16 g, bf16 weight copy)", "n": n,
+           "step": {"ms": ms, "params/s": n / (ms / 1e3), "GB/s": 30 * n / ms / 1e6,
+                    "frac": 30 * n / ms / 1e6 / peak}}
+    print(json.dumps(row), flush=True)
+    del w, m, v, g16, w_lp
+    torch.cuda.empty_cache()
+
     # latency case: 65,536 parameters (L2-resident), plain launches vs graph
     wl = W.flat_65k()
     n = wl.n

@@ -66,6 +66,11 @@ extern "C" {
 /* adamw_create flags. */
 #define ADAMW_CREATE_NO_CKPT 1 /* do not allocate the checkpoint staging    */
 
+/* Element types of adamw_clip_step_mixed's gradient and weight copy. */
+#define ADAMW_DTYPE_F32 0  /* IEEE binary32                               */
+#define ADAMW_DTYPE_BF16 1 /* bfloat16: the top 16 bits of a binary32      */
+#define ADAMW_DTYPE_F16 2  /* IEEE binary16                                */
+
 /* adamw_set_launch_options flags. */
 #define ADAMW_LAUNCH_NO_PDL 1 /* launch the fused kernel after the norm ends  */
 
@@ -178,6 +183,30 @@ ADAMW_API int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* 
                                  float* d_v, int32_t t, double lr, double wd,
                                  double clip, double grad_scale, double global_sumsq,
                                  int32_t flags, void* stream);
+
+/*
+ * The mixed-precision step ([B] "Where the gradients live": FP16 gradient
+ * buffers, ~240 MB at FP16 for 120M parameters; "Framework overhead": the
+ * FP16 cuBLAS path).  Weights (the float32 master copy), m and v stay
+ * float32 -- they are what step_NNNNNN.bin stores; the gradient d_g has
+ * g_dtype (ADAMW_DTYPE_F32 / _BF16 / _F16), read and widened exactly; if
+ * d_w_lp is not NULL the new weights are also written there rounded to
+ * w_lp_dtype (BF16 or F16, nearest even), the copy the next forward pass
+ * reads.  Everything else is as adamw_clip_step_ex (grad_scale,
+ * global_sumsq, ADAMW_ZERO_GRAD zeroes the 16-bit g, ADAMW_TENSOR_NORMS).
+ * Bytes per parameter with a 16-bit g and a copy: 2 (norm) + 2 + 12 read,
+ * 12 + 2 written.  16-bit types or a copy need w, m, v on 16-byte
+ * boundaries and d_g (16-bit) and d_w_lp on 8-byte boundaries.
+ */
+ADAMW_API int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype,
+                                    float* d_m, float* d_v, void* d_w_lp,
+                                    int32_t w_lp_dtype, int32_t t, double lr, double wd,
+                                    double clip, double grad_scale, double global_sumsq,
+                                    int32_t flags, void* stream);
+
+/* grad_sumsq for a gradient of element type g_dtype (16-bit: 8-byte aligned). */
+ADAMW_API int grad_sumsq_typed(adamw_ctx* ctx, const void* d_g, int32_t g_dtype,
+                               double* h_sumsq, void* stream);
 
 /*
  * Sum of g^2 over this context's n values of d_g (double, the same

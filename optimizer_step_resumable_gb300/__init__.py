@@ -21,6 +21,7 @@ OK = 0
 EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9, -1)
 CREATE_NO_CKPT = 1
 CKPT_DIRECT = 1
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 ZERO_GRAD = 1
 TENSOR_NORMS = 2
 LAUNCH_NO_PDL = 1
@@ -46,6 +47,10 @@ SIGNATURES = {
                                       _c.c_int32, _vp]),
     "grad_sumsq": (_c.c_int, [_vp, _vp, _c.POINTER(_c.c_double), _vp]),
     "grad_tensor_sumsq": (_c.c_int, [_vp, _vp, _vp, _vp]),
+    "adamw_clip_step_mixed": (_c.c_int, [_vp, _vp, _vp, _c.c_int32, _vp, _vp, _vp, _c.c_int32,
+                                         _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
+                                         _c.c_double, _c.c_double, _c.c_int32, _vp]),
+    "grad_sumsq_typed": (_c.c_int, [_vp, _vp, _c.c_int32, _c.POINTER(_c.c_double), _vp]),
     "adamw_last_tensor_sumsq": (_c.c_int, [_vp, _vp]),
     "adamw_graph_create": (_c.c_int, [_vp, _vp, _vp, _vp, _vp]),
     "adamw_graph_step": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
@@ -245,6 +250,50 @@ def adamw_clip_step_ex(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, c
         _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip), float(grad_scale),
         float(global_sumsq), flags, _stream(stream))
     _check(st, "adamw_clip_step_ex")
+
+
+def _dtype_of(t):
+    import torch
+    table = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}
+    if t.dtype not in table:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return table[t.dtype]
+
+
+def _typed_ptr(t, n: int, name: str) -> int:
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA tensor")
+    if t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} elements, context has {n}")
+    return t.data_ptr()
+
+
+def adamw_clip_step_mixed(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, clip: float,
+                          w_lp=None, grad_scale: float = 1.0, global_sumsq: float = -1.0,
+                          zero_grad: bool = False, tensor_norms: bool = False, stream=None):
+    """Float32 master w, m, v; g float32/bfloat16/float16; optional 16-bit
+    copy w_lp (bfloat16 or float16 tensor) of the new weights."""
+    n = ctx.n
+    flags = (ZERO_GRAD if zero_grad else 0) | (TENSOR_NORMS if tensor_norms else 0)
+    lp_ptr, lp_dt = None, DTYPE_BF16
+    if w_lp is not None:
+        lp_ptr, lp_dt = _typed_ptr(w_lp, n, "w_lp"), _dtype_of(w_lp)
+        if lp_dt == DTYPE_F32:
+            raise TypeError("w_lp must be bfloat16 or float16")
+    st = library().adamw_clip_step_mixed(
+        ctx.handle, _dev_ptr(w, n, "w"), _typed_ptr(g, n, "g"), _dtype_of(g), _dev_ptr(m, n, "m"),
+        _dev_ptr(v, n, "v"), lp_ptr, lp_dt, int(t), float(lr), float(wd), float(clip),
+        float(grad_scale), float(global_sumsq), flags, _stream(stream))
+    _check(st, "adamw_clip_step_mixed")
+
+
+def grad_sumsq_typed(ctx: Context, g, stream=None) -> float:
+    out = ctypes.c_double()
+    st = library().grad_sumsq_typed(ctx.handle, _typed_ptr(g, ctx.n, "g"), _dtype_of(g),
+                                    ctypes.byref(out), _stream(stream))
+    _check(st, "grad_sumsq_typed")
+    return out.value
 
 
 def grad_tensor_sumsq(ctx: Context, g, stream=None):

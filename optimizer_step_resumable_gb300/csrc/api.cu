@@ -124,13 +124,14 @@ int validate_table(int64_t n, const int64_t* offsets, const int64_t* numels, int
     return ADAMW_OK;
 }
 
-int launch_norm_on(adamw_ctx* c, const float* g, double clip, void* stream,
-                   double grad_scale = 1.0, bool tensor_sums = false)
+int launch_norm_on(adamw_ctx* c, const void* g, double clip, void* stream,
+                   double grad_scale = 1.0, bool tensor_sums = false,
+                   int32_t g_dtype = ADAMW_DTYPE_F32)
 {
     const osr::TensorSegs segs{c->d_tab_offsets, c->d_kfirst, c->d_segbase, c->d_seg_sums};
     const int e = osr::launch_norm(g, c->n, clip, c->d_partials, c->d_counter, c->d_res,
                                    c->h_res_dev, stream, grad_scale,
-                                   tensor_sums ? &segs : nullptr);
+                                   tensor_sums ? &segs : nullptr, g_dtype);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "norm kernel launch");
     c->segs_launched = tensor_sums;
@@ -394,13 +395,42 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
                        int32_t t, double lr, double wd, double clip, double grad_scale,
                        double global_sumsq, int32_t flags, void* stream)
 {
+    return adamw_clip_step_mixed(ctx, d_w, d_g, ADAMW_DTYPE_F32, d_m, d_v, nullptr,
+                                 ADAMW_DTYPE_BF16, t, lr, wd, clip, grad_scale, global_sumsq,
+                                 flags, stream);
+}
+
+int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m,
+                          float* d_v, void* d_w_lp, int32_t w_lp_dtype, int32_t t, double lr,
+                          double wd, double clip, double grad_scale, double global_sumsq,
+                          int32_t flags, void* stream)
+{
     osr::clear_error();
     if (!ctx)
         return fail(ADAMW_EINVAL, "ctx is NULL");
     int rc;
-    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_g, "d_g")) ||
-        (rc = check_state_ptr(d_m, "d_m")) || (rc = check_state_ptr(d_v, "d_v")))
+    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_m, "d_m")) ||
+        (rc = check_state_ptr(d_v, "d_v")))
         return rc;
+    if (g_dtype != ADAMW_DTYPE_F32 && g_dtype != ADAMW_DTYPE_BF16 && g_dtype != ADAMW_DTYPE_F16)
+        return fail(ADAMW_EINVAL, "g_dtype=%d is not F32, BF16 or F16", g_dtype);
+    if (d_w_lp && w_lp_dtype != ADAMW_DTYPE_BF16 && w_lp_dtype != ADAMW_DTYPE_F16)
+        return fail(ADAMW_EINVAL, "w_lp_dtype=%d is not BF16 or F16", w_lp_dtype);
+    if (!d_g)
+        return fail(ADAMW_EINVAL, "d_g is NULL");
+    if (g_dtype == ADAMW_DTYPE_F32 && !d_w_lp) {
+        if ((rc = check_state_ptr(d_g, "d_g")))
+            return rc;
+    } else {
+        const uintptr_t ga = reinterpret_cast<uintptr_t>(d_g);
+        if ((reinterpret_cast<uintptr_t>(d_w) | reinterpret_cast<uintptr_t>(d_m) |
+             reinterpret_cast<uintptr_t>(d_v)) & 15u ||
+            (g_dtype == ADAMW_DTYPE_F32 ? (ga & 15u) : (ga & 7u)) ||
+            (reinterpret_cast<uintptr_t>(d_w_lp) & 7u))
+            return fail(ADAMW_EINVAL,
+                        "16-bit gradients or a weight copy need w, m, v (and a float32 g) on "
+                        "16-byte boundaries, a 16-bit g and the copy on 8-byte boundaries");
+    }
     if (t < 1)
         return fail(ADAMW_EINVAL, "t=%d: the first update has t = 1", t);
     if (!(lr >= 0.0 && std::isfinite(lr)) || !(wd >= 0.0 && std::isfinite(wd)))
@@ -431,7 +461,7 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
         CUDA_TRY(cudaEventRecord(prof[0], st));
     if (!external) {
         rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale,
-                            (flags & ADAMW_TENSOR_NORMS) != 0);
+                            (flags & ADAMW_TENSOR_NORMS) != 0, g_dtype);
         if (rc != ADAMW_OK)
             return rc;
     }
@@ -442,7 +472,7 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
     const bool programmatic = !external && !prof[1] && ctx->pdl;
     const int e = osr::launch_adamw(d_w, d_g, d_m, d_v, ctx->n, k, external ? nullptr : ctx->d_res,
                                     ctx->caps, stream, (flags & ADAMW_ZERO_GRAD) != 0,
-                                    programmatic);
+                                    programmatic, g_dtype, d_w_lp, w_lp_dtype);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "clip+AdamW kernel launch");
     if (prof[2])
@@ -494,14 +524,26 @@ int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags)
 
 int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream)
 {
+    return grad_sumsq_typed(ctx, d_g, ADAMW_DTYPE_F32, h_sumsq, stream);
+}
+
+int grad_sumsq_typed(adamw_ctx* ctx, const void* d_g, int32_t g_dtype, double* h_sumsq,
+                     void* stream)
+{
     osr::clear_error();
     if (!ctx || !h_sumsq)
         return fail(ADAMW_EINVAL, "ctx or h_sumsq is NULL");
-    int rc = check_state_ptr(d_g, "d_g");
+    int rc = ADAMW_OK;
+    if (g_dtype == ADAMW_DTYPE_F32)
+        rc = check_state_ptr(d_g, "d_g");
+    else if (g_dtype != ADAMW_DTYPE_BF16 && g_dtype != ADAMW_DTYPE_F16)
+        rc = fail(ADAMW_EINVAL, "g_dtype=%d is not F32, BF16 or F16", g_dtype);
+    else if (!d_g || (reinterpret_cast<uintptr_t>(d_g) & 7u))
+        rc = fail(ADAMW_EINVAL, "a 16-bit d_g must be on an 8-byte boundary");
     if (rc != ADAMW_OK)
         return rc;
     DeviceScope scope(ctx->device);
-    rc = launch_norm_on(ctx, d_g, INFINITY, stream);
+    rc = launch_norm_on(ctx, d_g, INFINITY, stream, 1.0, false, g_dtype);
     if (rc == ADAMW_OK)
         rc = mark_norm(ctx, static_cast<cudaStream_t>(stream));
     if (rc != ADAMW_OK)

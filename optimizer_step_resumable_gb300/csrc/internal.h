@@ -91,13 +91,22 @@ inline int64_t norm_block_tile(int64_t n, int b)
 // The norm kernel publishes norm = grad_scale sqrt(sum g^2) and the factor
 // applied to g: grad_scale * (norm > clip ? clip / norm : 1); with segs, also
 // the per-tensor segment sums.
-int launch_norm(const float* g, int64_t n, double clip, double* partials,
+// Element types of the gradient and of the optional 16-bit weight copy.
+constexpr int32_t kDtypeF32 = 0, kDtypeBF16 = 1, kDtypeF16 = 2;
+
+int launch_norm(const void* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream, double grad_scale = 1.0, const TensorSegs* segs = nullptr);
-int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
+                void* stream, double grad_scale = 1.0, const TensorSegs* segs = nullptr,
+                int32_t g_dtype = kDtypeF32);
+// g of type g_dtype (16-byte aligned for float32 on the vector path, 8-byte
+// for 16-bit types); w_lp (may be NULL) receives the new weights rounded to
+// w_lp_dtype (bfloat16 or binary16; 8-byte aligned).  16-bit types and the
+// copy need 16-byte aligned w, m, v.
+int launch_adamw(float* w, const void* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res,
                  const KernelCaps& caps, void* stream, bool zero_grad = false,
-                 bool programmatic = false);
+                 bool programmatic = false, int32_t g_dtype = kDtypeF32,
+                 void* w_lp = nullptr, int32_t w_lp_dtype = kDtypeBF16);
 int launch_pack(const float* w, const float* m, const float* v, int64_t n,
                 int32_t step, unsigned char* image, const KernelCaps& caps,
                 void* stream);
@@ -123,7 +132,8 @@ struct AdamwNodeArgs {
     int64_t n;
     StepScalars k;
     const NormResult* d_res;
-    void* ptrs[7];
+    void* w_lp;  // always NULL in the step graph
+    void* ptrs[8];
 };
 }  // namespace osr
 struct cudaKernelNodeParams;

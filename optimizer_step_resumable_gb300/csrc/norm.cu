@@ -114,9 +114,9 @@ __device__ __forceinline__ double thread_sumsq_in(const float4 (&x)[U], int64_t 
 // ---------------------------------------------------------------------------
 // (at least 4 resident blocks per SM, so that the fixed 608-block grid is one
 // wave on 152 SMs whichever variant runs)
-template <bool kVec, bool kSegs>
+template <bool kVec, bool kSegs, typename G>
 __global__ void __launch_bounds__(kNormThreads, 4)
-    k_grad_norm(const float* __restrict__ g, int64_t n, double clip, double grad_scale,
+    k_grad_norm(const G* __restrict__ g, int64_t n, double clip, double grad_scale,
                 double* __restrict__ partials, unsigned int* __restrict__ counter,
                 NormResult* __restrict__ d_res, NormResult* h_res, TensorSegs segs)
 {
@@ -143,15 +143,14 @@ __global__ void __launch_bounds__(kNormThreads, 4)
         const int64_t base = tile * kNormTileElems;
         float4 x[U];
         if (tile < nfull) {
-            if (kVec) {
-                const float4* p = reinterpret_cast<const float4*>(g + base) + tid;
+            if constexpr (kVec) {
 #pragma unroll
                 for (int j = 0; j < U; ++j)
-                    x[j] = __ldcs(p + j * kNormThreads);
-            } else {
+                    x[j] = detail::load4_cs<G>(g + base + (int64_t(j * kNormThreads + tid) << 2));
+            } else {  // float32 at a 4-byte (not 16-byte) boundary
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
-                    const float* p = g + base + (int64_t(j * kNormThreads + tid) << 2);
+                    const G* p = g + base + (int64_t(j * kNormThreads + tid) << 2);
                     x[j] = make_float4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
                 }
             }
@@ -159,10 +158,10 @@ __global__ void __launch_bounds__(kNormThreads, 4)
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 const int64_t e = base + (int64_t(j * kNormThreads + tid) << 2);
-                x[j].x = e < n ? g[e] : 0.0f;
-                x[j].y = e + 1 < n ? g[e + 1] : 0.0f;
-                x[j].z = e + 2 < n ? g[e + 2] : 0.0f;
-                x[j].w = e + 3 < n ? g[e + 3] : 0.0f;
+                x[j].x = e < n ? detail::load1(g + e) : 0.0f;
+                x[j].y = e + 1 < n ? detail::load1(g + e + 1) : 0.0f;
+                x[j].z = e + 2 < n ? detail::load1(g + e + 2) : 0.0f;
+                x[j].w = e + 3 < n ? detail::load1(g + e + 3) : 0.0f;
             }
         }
         const double r = run_sumsq<U>(x);
@@ -240,29 +239,47 @@ __global__ void __launch_bounds__(kNormThreads, 4)
 
 }  // namespace
 
-int launch_norm(const float* g, int64_t n, double clip, double* partials,
-                unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream, double grad_scale, const TensorSegs* segs)
+namespace {
+
+template <typename G, bool kVec>
+void launch_norm_typed(const void* g, int64_t n, double clip, double* partials,
+                       unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                       cudaStream_t s, double grad_scale, const TensorSegs* segs)
 {
     const int blocks = norm_blocks(n);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const TensorSegs none{nullptr, nullptr, nullptr, nullptr};
-    const TensorSegs sg = segs ? *segs : none;
-    const bool vec = detail::aligned16(g);
-    if (segs) {
-        if (vec)
-            k_grad_norm<true, true><<<blocks, kNormThreads, 0, s>>>(
-                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+    const G* gt = static_cast<const G*>(g);
+    if (segs)
+        k_grad_norm<kVec, true, G><<<blocks, kNormThreads, 0, s>>>(
+            gt, n, clip, grad_scale, partials, counter, d_res, h_res_dev, *segs);
+    else
+        k_grad_norm<kVec, false, G><<<blocks, kNormThreads, 0, s>>>(
+            gt, n, clip, grad_scale, partials, counter, d_res, h_res_dev, none);
+}
+
+}  // namespace
+
+int launch_norm(const void* g, int64_t n, double clip, double* partials,
+                unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                void* stream, double grad_scale, const TensorSegs* segs, int32_t g_dtype)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (g_dtype) {
+    case kDtypeBF16:  // 8-byte alignment checked by the caller
+        launch_norm_typed<__nv_bfloat16, true>(g, n, clip, partials, counter, d_res, h_res_dev,
+                                               s, grad_scale, segs);
+        break;
+    case kDtypeF16:
+        launch_norm_typed<__half, true>(g, n, clip, partials, counter, d_res, h_res_dev, s,
+                                        grad_scale, segs);
+        break;
+    default:
+        if (detail::aligned16(g))
+            launch_norm_typed<float, true>(g, n, clip, partials, counter, d_res, h_res_dev, s,
+                                           grad_scale, segs);
         else
-            k_grad_norm<false, true><<<blocks, kNormThreads, 0, s>>>(
-                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
-    } else {
-        if (vec)
-            k_grad_norm<true, false><<<blocks, kNormThreads, 0, s>>>(
-                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
-        else
-            k_grad_norm<false, false><<<blocks, kNormThreads, 0, s>>>(
-                g, n, clip, grad_scale, partials, counter, d_res, h_res_dev, sg);
+            launch_norm_typed<float, false>(g, n, clip, partials, counter, d_res, h_res_dev, s,
+                                            grad_scale, segs);
     }
     return int(cudaGetLastError());
 }
@@ -279,8 +296,8 @@ int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p)
     a->ptrs[7] = &a->h_res;
     a->segs = TensorSegs{nullptr, nullptr, nullptr, nullptr};
     a->ptrs[8] = &a->segs;
-    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true, false>)
-                                      : reinterpret_cast<void*>(&k_grad_norm<false, false>);
+    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true, false, float>)
+                                      : reinterpret_cast<void*>(&k_grad_norm<false, false, float>);
     p->gridDim = dim3(unsigned(norm_blocks(a->n)));
     p->blockDim = dim3(kNormThreads);
     p->sharedMemBytes = 0;

@@ -11,6 +11,7 @@
 // Language Model: Backprop" is folded in).  HBM-bound: 28 bytes per
 // parameter (read w, g, m, v; write w, m, v).
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda_runtime.h>
 
@@ -55,18 +56,22 @@ __device__ __forceinline__ void adamw4(float4& w, float4 g, float4& m, float4& v
 constexpr int kStepThreads = 256;
 constexpr int kStepVec = 2;  // float4 of each array per thread per chunk
 
-// Reads w, g, m, v once and writes w, m, v once (28 bytes per parameter).
-// The clip factor and the non-finite flag come from the norm kernel's
-// result in device memory, so nothing returns to the host between kernels;
-// with res == nullptr the factor is k.scale (the host computed it from a
-// global sum of squares).  kZero also writes 0 into g after reading it
-// ("zero_grads" for the next accumulation), +4 bytes per parameter.
-template <bool kVec, bool kZero>
+// Reads w, g, m, v once and writes w, m, v once (28 bytes per parameter
+// with a float32 gradient).  The clip factor and the non-finite flag come
+// from the norm kernel's result in device memory, so nothing returns to the
+// host between kernels; with res == nullptr the factor is k.scale (the host
+// computed it from a global sum of squares).  G is the gradient's element
+// type (float, bfloat16, binary16; widened exactly).  kZero also writes 0
+// into g after reading it ("zero_grads" for the next accumulation).  WL, if
+// not void, is the type of a 16-bit copy of the new weights written to w_lp
+// (rounded to nearest even) for the next forward pass.
+template <bool kVec, bool kZero, typename G, typename WL>
 __global__ void __launch_bounds__(kStepThreads)
-    k_clip_adamw(float* __restrict__ w, const float* __restrict__ g,
+    k_clip_adamw(float* __restrict__ w, const G* __restrict__ g,
                  float* __restrict__ m, float* __restrict__ v, int64_t n,
-                 StepScalars k, const NormResult* __restrict__ res)
+                 StepScalars k, const NormResult* __restrict__ res, WL* __restrict__ w_lp)
 {
+    constexpr bool kCopy = !std::is_void<WL>::value;
     // When launched right behind the norm kernel with programmatic
     // serialization, this grid may start while that kernel still runs: warm
     // L2 with this block's first chunk (inputs the norm kernel does not
@@ -93,98 +98,86 @@ __global__ void __launch_bounds__(kStepThreads)
         s = res->scale;
     }
     // written through the same restrict pointer it is read from
-    float* const gw = const_cast<float*>(g);
+    G* const gw = const_cast<G*>(g);
     const int64_t gtid = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
     const int64_t stride = int64_t(gridDim.x) * kStepThreads;
-    if (kVec) {
+    if constexpr (kVec) {
         float4* w4 = reinterpret_cast<float4*>(w);
-        const float4* g4 = reinterpret_cast<const float4*>(g);
-        float4* gw4 = reinterpret_cast<float4*>(gw);
         float4* m4 = reinterpret_cast<float4*>(m);
         float4* v4 = reinterpret_cast<float4*>(v);
-        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
         const int64_t n4 = n >> 2;
         constexpr int64_t chunk = int64_t(kStepThreads) * kStepVec;
         const int64_t nchunks = n4 / chunk;
         for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
             const int64_t i0 = c * chunk + threadIdx.x;
-            float4 W[kStepVec], G[kStepVec], M[kStepVec], V[kStepVec];
+            float4 W[kStepVec], G4[kStepVec], M[kStepVec], V[kStepVec];
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j) {
                 const int64_t i = i0 + j * kStepThreads;
                 W[j] = __ldcs(w4 + i);
-                G[j] = __ldcs(g4 + i);
+                G4[j] = detail::load4_cs<G>(g + (i << 2));
                 M[j] = __ldcs(m4 + i);
                 V[j] = __ldcs(v4 + i);
             }
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j)
-                adamw4(W[j], G[j], M[j], V[j], s, k);
+                adamw4(W[j], G4[j], M[j], V[j], s, k);
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j) {
                 const int64_t i = i0 + j * kStepThreads;
                 __stcs(w4 + i, W[j]);
                 __stcs(m4 + i, M[j]);
                 __stcs(v4 + i, V[j]);
-                if (kZero)
-                    __stcs(gw4 + i, zero4);
+                if constexpr (kZero)
+                    detail::store4_zero_cs(gw + (i << 2));
+                if constexpr (kCopy)
+                    detail::store4_lp_cs(w_lp + (i << 2), W[j]);
             }
         }
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
-            float4 W = __ldcs(w4 + i), G = __ldcs(g4 + i), M = __ldcs(m4 + i),
-                   V = __ldcs(v4 + i);
-            adamw4(W, G, M, V, s, k);
+            float4 W = __ldcs(w4 + i), G4 = detail::load4_cs<G>(g + (i << 2)),
+                   M = __ldcs(m4 + i), V = __ldcs(v4 + i);
+            adamw4(W, G4, M, V, s, k);
             __stcs(w4 + i, W);
             __stcs(m4 + i, M);
             __stcs(v4 + i, V);
-            if (kZero)
-                __stcs(gw4 + i, zero4);
+            if constexpr (kZero)
+                detail::store4_zero_cs(gw + (i << 2));
+            if constexpr (kCopy)
+                detail::store4_lp_cs(w_lp + (i << 2), W);
         }
         if (gtid < (n & 3)) {
             const int64_t e = (n4 << 2) + gtid;
             float W = w[e], M = m[e], V = v[e];
-            adamw_elem(W, g[e], M, V, s, k);
+            adamw_elem(W, detail::load1(g + e), M, V, s, k);
             w[e] = W;
             m[e] = M;
             v[e] = V;
-            if (kZero)
-                gw[e] = 0.0f;
+            if constexpr (kZero)
+                detail::store1_zero(gw + e);
+            if constexpr (kCopy)
+                detail::store1_lp(w_lp + e, W);
         }
-    } else {
+    } else {  // float32 state at 4-byte boundaries, float32 gradient, no copy
         for (int64_t e = gtid; e < n; e += stride) {
             float W = __ldcs(w + e), M = __ldcs(m + e), V = __ldcs(v + e);
             adamw_elem(W, __ldcs(g + e), M, V, s, k);
             __stcs(w + e, W);
             __stcs(m + e, M);
             __stcs(v + e, V);
-            if (kZero)
+            if constexpr (kZero)
                 __stcs(gw + e, 0.0f);
         }
     }
 }
 
-}  // namespace
-
-int query_step_caps(int sm_count, KernelCaps* caps)
-{
-    // the zeroing variants have the same shape; their counts are not needed
-    cudaError_t err = cudaSuccess;
-    caps->step_vec = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<true, false>), kStepThreads, sm_count, &err);
-    caps->step_scalar = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<false, false>), kStepThreads, sm_count, &err);
-    return int(err);
-}
-
-namespace {
-
 // Launches the fused kernel; with `programmatic`, as a programmatic
 // dependent of the kernel before it in the stream (that kernel must be the
 // norm reduction, whose blocks release it early).
-template <typename Kernel>
-void launch_step(Kernel kernel, int blocks, cudaStream_t s, bool programmatic, float* w,
-                 const float* g, float* m, float* v, int64_t n, const StepScalars& k,
-                 const NormResult* d_res)
+template <bool kVec, bool kZero, typename G, typename WL>
+void launch_step(int blocks, cudaStream_t s, bool programmatic, float* w, const void* g,
+                 float* m, float* v, int64_t n, const StepScalars& k, const NormResult* d_res,
+                 void* w_lp)
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(blocks));
@@ -196,37 +189,86 @@ void launch_step(Kernel kernel, int blocks, cudaStream_t s, bool programmatic, f
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    cudaLaunchKernelEx(&cfg, kernel, w, g, m, v, n, k, d_res);  // status: cudaGetLastError
+    // status: cudaGetLastError in the caller
+    cudaLaunchKernelEx(&cfg, &k_clip_adamw<kVec, kZero, G, WL>, w, static_cast<const G*>(g), m,
+                       v, n, k, d_res, static_cast<WL*>(w_lp));
+}
+
+template <bool kZero, typename G>
+void launch_vec(int blocks, cudaStream_t s, bool pdl, float* w, const void* g, float* m,
+                float* v, int64_t n, const StepScalars& k, const NormResult* d_res, void* w_lp,
+                int32_t w_lp_dtype)
+{
+    if (!w_lp)
+        launch_step<true, kZero, G, void>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp);
+    else if (w_lp_dtype == kDtypeF16)
+        launch_step<true, kZero, G, __half>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp);
+    else
+        launch_step<true, kZero, G, __nv_bfloat16>(blocks, s, pdl, w, g, m, v, n, k, d_res,
+                                                   w_lp);
+}
+
+template <bool kZero>
+void launch_vec_any(int32_t g_dtype, int blocks, cudaStream_t s, bool pdl, float* w,
+                    const void* g, float* m, float* v, int64_t n, const StepScalars& k,
+                    const NormResult* d_res, void* w_lp, int32_t w_lp_dtype)
+{
+    if (g_dtype == kDtypeBF16)
+        launch_vec<kZero, __nv_bfloat16>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
+                                         w_lp_dtype);
+    else if (g_dtype == kDtypeF16)
+        launch_vec<kZero, __half>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp, w_lp_dtype);
+    else
+        launch_vec<kZero, float>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp, w_lp_dtype);
 }
 
 }  // namespace
 
-int launch_adamw(float* w, const float* g, float* m, float* v, int64_t n,
+int query_step_caps(int sm_count, KernelCaps* caps)
+{
+    // the other variants have the same shape and the same register budget
+    cudaError_t err = cudaSuccess;
+    caps->step_vec = detail::resident_blocks(
+        reinterpret_cast<const void*>(&k_clip_adamw<true, false, float, void>), kStepThreads,
+        sm_count, &err);
+    caps->step_scalar = detail::resident_blocks(
+        reinterpret_cast<const void*>(&k_clip_adamw<false, false, float, void>), kStepThreads,
+        sm_count, &err);
+    return int(err);
+}
+
+int launch_adamw(float* w, const void* g, float* m, float* v, int64_t n,
                  const StepScalars& k, const NormResult* d_res, const KernelCaps& caps,
-                 void* stream, bool zero_grad, bool programmatic)
+                 void* stream, bool zero_grad, bool programmatic, int32_t g_dtype, void* w_lp,
+                 int32_t w_lp_dtype)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool vec = detail::aligned16(w) && detail::aligned16(g) && detail::aligned16(m) &&
-                     detail::aligned16(v);
+    const bool plain = g_dtype == kDtypeF32 && !w_lp;
+    const bool vec = detail::aligned16(w) && detail::aligned16(m) && detail::aligned16(v) &&
+                     (g_dtype == kDtypeF32 ? detail::aligned16(g) : detail::aligned8(g)) &&
+                     (!w_lp || detail::aligned8(w_lp));
+    if (!vec && !plain)
+        return int(cudaErrorMisalignedAddress);  // callers refuse this before launching
     if (vec) {
         const int cap = caps.step_vec;
         const int64_t want = detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
         if (zero_grad)
-            launch_step(&k_clip_adamw<true, true>, blocks, s, programmatic, w, g, m, v, n, k, d_res);
+            launch_vec_any<true>(g_dtype, blocks, s, programmatic, w, g, m, v, n, k, d_res, w_lp,
+                                 w_lp_dtype);
         else
-            launch_step(&k_clip_adamw<true, false>, blocks, s, programmatic, w, g, m, v, n, k,
-                        d_res);
+            launch_vec_any<false>(g_dtype, blocks, s, programmatic, w, g, m, v, n, k, d_res,
+                                  w_lp, w_lp_dtype);
     } else {
         const int cap = caps.step_scalar;
         const int64_t want = detail::ceil_div(n, kStepThreads);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
         if (zero_grad)
-            launch_step(&k_clip_adamw<false, true>, blocks, s, programmatic, w, g, m, v, n, k,
-                        d_res);
+            launch_step<false, true, float, void>(blocks, s, programmatic, w, g, m, v, n, k,
+                                                  d_res, nullptr);
         else
-            launch_step(&k_clip_adamw<false, false>, blocks, s, programmatic, w, g, m, v, n, k,
-                        d_res);
+            launch_step<false, false, float, void>(blocks, s, programmatic, w, g, m, v, n, k,
+                                                   d_res, nullptr);
     }
     return int(cudaGetLastError());
 }
@@ -240,16 +282,18 @@ int adamw_node_params(AdamwNodeArgs* a, const KernelCaps& caps, cudaKernelNodePa
     a->ptrs[4] = &a->n;
     a->ptrs[5] = &a->k;
     a->ptrs[6] = &a->d_res;
+    a->w_lp = nullptr;
+    a->ptrs[7] = &a->w_lp;
     const bool vec = detail::aligned16(a->w) && detail::aligned16(a->g) &&
                      detail::aligned16(a->m) && detail::aligned16(a->v);
     int64_t want;
     int cap;
     if (vec) {
-        p->func = reinterpret_cast<void*>(&k_clip_adamw<true, false>);
+        p->func = reinterpret_cast<void*>(&k_clip_adamw<true, false, float, void>);
         want = detail::ceil_div(a->n >> 2, int64_t(kStepThreads) * kStepVec);
         cap = caps.step_vec;
     } else {
-        p->func = reinterpret_cast<void*>(&k_clip_adamw<false, false>);
+        p->func = reinterpret_cast<void*>(&k_clip_adamw<false, false, float, void>);
         want = detail::ceil_div(a->n, kStepThreads);
         cap = caps.step_scalar;
     }

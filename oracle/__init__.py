@@ -99,6 +99,15 @@ class Oracle:
             c.c_double, c.c_double, c.c_double, c.c_double, c.c_double,
             c.c_double, c.POINTER(c.c_double)]
         lib.oracle_adamw_clip_step_scaled.restype = c.c_int
+        lib.oracle_decode16.argtypes = [c.c_uint16, c.c_int32]
+        lib.oracle_decode16.restype = c.c_double
+        lib.oracle_encode16.argtypes = [c.c_float, c.c_int32]
+        lib.oracle_encode16.restype = c.c_uint16
+        lib.oracle_adamw_clip_step_mixed.argtypes = [
+            _f32p, c.c_void_p, c.c_int32, _f32p, _f32p, c.c_void_p, c.c_int32,
+            c.c_int64, c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
+            c.c_double, c.c_double, c.c_double, c.POINTER(c.c_double)]
+        lib.oracle_adamw_clip_step_mixed.restype = c.c_int
         lib.oracle_adamw_at.argtypes = [
             _i64p, c.c_int64, _f32p, _f32p, _f32p, _f32p, c.c_double,
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
@@ -188,6 +197,39 @@ class Oracle:
         if st not in (OK, ENONFINITE) or (st != OK and raise_on_error):
             raise OracleError(st, "oracle_adamw_clip_step_scaled")
         return st, norm.value
+
+    # 16-bit formats: dtype 0 = float32, 1 = bfloat16, 2 = IEEE binary16
+    def decode16(self, h: int, dtype: int) -> float:
+        return self._lib.oracle_decode16(int(h), int(dtype))
+
+    def encode16(self, x: float, dtype: int) -> int:
+        return self._lib.oracle_encode16(float(x), int(dtype))
+
+    def adamw_clip_step_mixed(self, w, g, g_dtype, m, v, t, lr, wd, clip,
+                              grad_scale=1.0, w_lp_dtype=None, beta1=BETA1,
+                              beta2=BETA2, eps=EPS, raise_on_error=True):
+        """In-place step with g given as float32 (g_dtype 0) or as uint16
+        bit patterns (1 = bfloat16, 2 = binary16); returns (status, norm,
+        w_lp) where w_lp holds the new weights rounded to w_lp_dtype."""
+        for a in (w, m, v):
+            _check_inplace(a)
+        if g_dtype == 0:
+            g = np.ascontiguousarray(g, dtype=np.float32)
+        else:
+            g = np.ascontiguousarray(g, dtype=np.uint16)
+        if g.size != w.size:
+            raise ValueError("g size")
+        w_lp = None if w_lp_dtype is None else np.empty(w.size, np.uint16)
+        norm = ctypes.c_double()
+        st = self._lib.oracle_adamw_clip_step_mixed(
+            w, g.ctypes.data, int(g_dtype), m, v,
+            None if w_lp is None else w_lp.ctypes.data,
+            0 if w_lp_dtype is None else int(w_lp_dtype), w.size, int(t), float(lr),
+            float(wd), float(clip), float(grad_scale), float(beta1), float(beta2),
+            float(eps), ctypes.byref(norm))
+        if st not in (OK, ENONFINITE) or (st != OK and raise_on_error):
+            raise OracleError(st, "oracle_adamw_clip_step_mixed")
+        return st, norm.value, w_lp
 
     def adamw_at(self, idx, w, g, m, v, s, t, lr, wd, beta1=BETA1,
                  beta2=BETA2, eps=EPS):

@@ -210,6 +210,125 @@ int oracle_adamw_clip_step_scaled(float* w, const float* g, float* m, float* v,
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------
+ * 16-bit formats of the mixed-precision step.  "Grow a Language Model:
+ * Backprop" (unhomeschool.com): FP16 gradient buffers (section "Where the
+ * gradients live": ~240 MB at FP16 for 120M parameters) and an FP16 cuBLAS
+ * path (section "Framework overhead").  The optimizer keeps float32 master
+ * weights and moments; gradients arrive in bfloat16 or IEEE binary16, and a
+ * 16-bit copy of the new weights is produced for the next forward pass.
+ * Decoding is exact; encoding rounds to nearest, ties to even.
+ *
+ * bfloat16: the top 16 bits of a binary32 value.
+ * binary16 (IEEE 754-2008): 1 sign bit, 5 exponent bits (bias 15), 10
+ * fraction bits; exponent 0 = zero or subnormal (fraction x 2^-24),
+ * exponent 31 = inf or nan.
+ * ---------------------------------------------------------------------- */
+#define DT_F32 0
+#define DT_BF16 1
+#define DT_F16 2
+
+double oracle_decode16(uint16_t h, int32_t dtype)
+{
+    if (dtype == DT_BF16) {
+        uint32_t bits = (uint32_t)h << 16;
+        float f;
+        memcpy(&f, &bits, 4);
+        return (double)f;
+    }
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 31;
+    int frac = h & 1023;
+    double mag;
+    if (ex == 0)
+        mag = ldexp((double)frac, -24);
+    else if (ex == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + frac), ex - 25);
+    return sign ? -mag : mag;
+}
+
+uint16_t oracle_encode16(float x, int32_t dtype)
+{
+    uint32_t bits;
+    memcpy(&bits, &x, 4);
+    if (dtype == DT_BF16) {
+        if ((bits & 0x7fffffffu) > 0x7f800000u)          /* nan: keep it a nan */
+            return (uint16_t)((bits >> 16) | 0x0040u);
+        uint32_t lsb = (bits >> 16) & 1u;
+        return (uint16_t)((bits + 0x7fffu + lsb) >> 16);  /* nearest, ties even */
+    }
+    /* binary16: nearest representable value, ties to the even fraction */
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    double a = fabs((double)x);
+    if (x != x)
+        return (uint16_t)(sign | 0x7e00u);
+    if (a >= 65520.0)                                    /* rounds past 65504 */
+        return (uint16_t)(sign | 0x7c00u);
+    /* step between neighbours at a: 2^-24 below 2^-14, else 2^(e-10) */
+    int e;
+    frexp(a, &e);                                        /* a = f 2^e, f in [0.5,1) */
+    int q = (e - 1 < -14) ? -24 : (e - 1) - 10;          /* exponent of one step */
+    double steps = ldexp(a, -q);                         /* exact: a is a float */
+    double fl = floor(steps);
+    double rem = steps - fl;
+    uint32_t k = (uint32_t)fl;
+    if (rem > 0.5 || (rem == 0.5 && (k & 1u)))
+        k += 1;
+    /* k steps of 2^q: rebuild the encoding */
+    double val = ldexp((double)k, q);
+    if (val == 0.0)
+        return sign;
+    int ve;
+    frexp(val, &ve);
+    if (ve - 1 < -14)                                    /* subnormal */
+        return (uint16_t)(sign | (uint16_t)k);
+    uint32_t exp_field = (uint32_t)(ve - 1 + 15);
+    uint32_t frac_field = (uint32_t)(ldexp(val, -(ve - 1)) * 1024.0 - 1024.0);
+    return (uint16_t)(sign | (exp_field << 10) | frac_field);
+}
+
+/* The step with a 16-bit (or float32) gradient and an optional 16-bit copy
+ * of the new weights: each gradient value decoded exactly, times
+ * grad_scale, then norm, clip and update as oracle_adamw_clip_step_scaled;
+ * w_lp (if not NULL) receives the new float32 weights rounded to w_lp_dtype. */
+int oracle_adamw_clip_step_mixed(float* w, const void* g, int32_t g_dtype, float* m,
+                                 float* v, uint16_t* w_lp, int32_t w_lp_dtype,
+                                 int64_t n, int32_t t, double lr, double wd,
+                                 double clip, double grad_scale, double beta1,
+                                 double beta2, double eps, double* norm_out)
+{
+    if (n < 0 || t < 1)
+        return OR_EINVAL;
+    double sumsq = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = g_dtype == DT_F32 ? (double)((const float*)g)[i]
+                                      : oracle_decode16(((const uint16_t*)g)[i], g_dtype);
+        double x = gi * grad_scale;
+        sumsq = sumsq + x * x;
+    }
+    double norm = sqrt(sumsq);
+    if (norm_out)
+        *norm_out = norm;
+    if (!isfinite(norm))
+        return OR_ENONFINITE;
+    double s = oracle_clip_scale(norm, clip);
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = g_dtype == DT_F32 ? (double)((const float*)g)[i]
+                                      : oracle_decode16(((const uint16_t*)g)[i], g_dtype);
+        oracle_terms r;
+        oracle_adamw_element((double)w[i], gi * grad_scale, (double)m[i],
+                             (double)v[i], s, t, lr, wd, beta1, beta2, eps, &r);
+        w[i] = (float)r.w;
+        m[i] = (float)r.m;
+        v[i] = (float)r.v;
+        if (w_lp)
+            w_lp[i] = oracle_encode16(w[i], w_lp_dtype);
+    }
+    return OR_OK;
+}
+
 /* The same update at chosen indices only, given the clip factor s (from a
  * full-vector norm computed separately).  Used to check outputs of a large
  * state one element at a time.  Results go to the *_out arrays. */

@@ -128,3 +128,16 @@ def device_args(seed: int, stream: int, step: int, sigma: float,
                 okey=stream_key(seed, STREAM_OUTLIER, step),
                 othr=outlier_threshold(outlier_frac),
                 omul=float(np.float32(outlier_mult)))
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns of float32 inputs (nearest, ties to even): how
+    the 16-bit gradients of the mixed-precision tests are prepared."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns of float32 inputs (numpy's conversion)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)

@@ -352,6 +352,78 @@ def pin_micro_batch_average(o, tmp):
         assert x.tobytes() == y.tobytes()
 
 
+# --- 16-bit formats of the mixed-precision step ------------------------------
+
+def pin_decode16_values(o, tmp):
+    """Hand-decoded bit patterns: bfloat16 is the top half of a binary32;
+    binary16 has bias 15, 10 fraction bits, subnormals at 2^-24 steps."""
+    for h, want in ((0x3F80, 1.0), (0xC000, -2.0), (0x3EAB, 0.333984375), (0x0001, 2.0 ** -133),
+                    (0x7F7F, 3.3895313892515355e38), (0x7F80, math.inf)):
+        assert o.decode16(h, 1) == want, hex(h)
+    for h, want in ((0x3C00, 1.0), (0x0001, 2.0 ** -24), (0x03FF, 1023 * 2.0 ** -24),
+                    (0x0400, 2.0 ** -14), (0x7BFF, 65504.0), (0xC000, -2.0),
+                    (0x3555, 0.333251953125), (0x7C00, math.inf), (0xFC00, -math.inf)):
+        assert o.decode16(h, 2) == want, hex(h)
+    assert math.isnan(o.decode16(0x7E00, 2)) and math.isnan(o.decode16(0x7FC0, 1))
+    assert math.copysign(1.0, o.decode16(0x8000, 2)) == -1.0
+
+
+def pin_encode_f16_matches_numpy(o, tmp):
+    """binary16 rounding equals numpy's float16 conversion (nearest, ties to
+    even) bit for bit, across subnormals, normals, ties and overflow."""
+    rng = np.random.default_rng(14)
+    x = np.concatenate([
+        (rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000)).astype(np.float32),
+        np.array([65504, 65519.99, 65520, 70000, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                  2.0 ** -14 - 2.0 ** -25, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 0.0, -0.0,
+                  np.inf, -np.inf], np.float32)])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    got = np.array([o.encode16(v, 2) for v in x], np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (x[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def pin_encode_bf16_nearest_even(o, tmp):
+    """bfloat16 rounding picks the nearer of the two neighbouring bfloat16
+    values (distances compared in double), ties to the even pattern."""
+    rng = np.random.default_rng(15)
+    x = (rng.standard_normal(5000) * 10.0 ** rng.integers(-30, 30, 5000)).astype(np.float32)
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 5 * 2.0 ** -8)], np.float32)
+    for v in np.concatenate([x, ties]):
+        bits = int(np.float32(v).view(np.uint32))
+        lo = bits >> 16
+        cands = [(lo, o.decode16(lo, 1)), (lo + 1, o.decode16(lo + 1, 1))]
+        d = [abs(c - float(v)) for _, c in cands]
+        if d[0] != d[1]:
+            want = cands[0][0] if d[0] < d[1] else cands[1][0]
+        else:
+            want = cands[0][0] if cands[0][0] % 2 == 0 else cands[1][0]
+        assert o.encode16(float(v), 1) == want, (v, hex(want))
+    assert [o.encode16(float(t), 1) for t in ties] == [0x3F80, 0x3F82, 0xBF82]
+
+
+def pin_mixed_step_equals_float32_step(o, tmp):
+    """Gradients exactly representable in 16 bits give the float32 step bit
+    for bit; the 16-bit weight copy is the rounding of the new weights."""
+    rng = np.random.default_rng(16)
+    n = 512
+    g32 = rng.integers(-64, 65, n).astype(np.float32) / np.float32(256)
+    g_bf = (g32.view(np.uint32) >> 16).astype(np.uint16)
+    g_f16 = g32.astype(np.float16).view(np.uint16)
+    for dt, g16 in ((1, g_bf), (2, g_f16)):
+        a = [rng.normal(0, 0.02, n).astype(np.float32), np.zeros(n, np.float32),
+             np.zeros(n, np.float32)]
+        b = [x.copy() for x in a]
+        _, n1, w_lp = o.adamw_clip_step_mixed(a[0], g16, dt, a[1], a[2], 1, 3e-3, 0.01, 1.0,
+                                              0.5, w_lp_dtype=dt)
+        _, n2 = o.adamw_clip_step_scaled(b[0], g32, b[1], b[2], 1, 3e-3, 0.01, 1.0, 0.5)
+        assert n1 == n2
+        for x, y in zip(a, b):
+            assert x.tobytes() == y.tobytes()
+        assert list(w_lp) == [o.encode16(float(x), dt) for x in a[0]]
+
+
 # --- checkpoint format -----------------------------------------------------
 
 def pin_ckpt_printed_sizes(o, tmp):

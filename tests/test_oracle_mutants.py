@@ -65,6 +65,15 @@ MUTANTS = {
                               "out[k] = oracle_sumsq(g + offsets[k], numels[k] - 1);"),
     "tensor_sum_shifted": ("out[k] = oracle_sumsq(g + offsets[k], numels[k]);",
                            "out[k] = oracle_sumsq(g + offsets[k] + 1, numels[k]);"),
+    "bf16_decode_shift": ("uint32_t bits = (uint32_t)h << 16;", "uint32_t bits = (uint32_t)h << 15;"),
+    "f16_decode_bias": ("mag = ldexp((double)(1024 + frac), ex - 25);",
+                        "mag = ldexp((double)(1024 + frac), ex - 24);"),
+    "f16_no_subnormal_scale": ("mag = ldexp((double)frac, -24);", "mag = ldexp((double)frac, -25);"),
+    "bf16_round_half_up": ("return (uint16_t)((bits + 0x7fffu + lsb) >> 16);",
+                           "return (uint16_t)((bits + 0x8000u) >> 16);"),
+    "f16_ties_away": ("if (rem > 0.5 || (rem == 0.5 && (k & 1u)))", "if (rem >= 0.5)"),
+    "f16_overflow_never": ("if (a >= 65520.0)", "if (a >= 1e300)"),
+    "mixed_ignores_scale": ("double x = gi * grad_scale;", "double x = gi;"),
     "scaled_clip_on_raw_norm": ("double x = (double)g[i] * grad_scale;\n        sumsq = sumsq + x * x;",
                                 "double x = (double)g[i];\n        sumsq = sumsq + x * x;"),
     "scaled_update_unscaled": ("oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,",
