@@ -43,7 +43,7 @@ struct StepScalars {
     float scale;            // gradient factor when no norm result is read
 };
 
-// Tunables of the kernels (fixed at compile time; see kernels.cu).
+// Tunables of the kernels (fixed at compile time; used in norm.cu, step.cu).
 constexpr int kNormThreads = 256;
 constexpr int kNormVecPerThread = 8;                 // float4 per thread per tile
 constexpr int64_t kNormTileElems = int64_t(kNormThreads) * kNormVecPerThread * 4;
