@@ -322,6 +322,7 @@ def run_ours(args):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
 
+    wait_s = []  # host time spent waiting for the previous checkpoint write
     sampler = ClockSampler(local, enabled=not args.no_clocks)
     time.sleep(0.3 if sampler.proc else 0)
     barrier(world)
@@ -330,6 +331,11 @@ def run_ours(args):
     for k in range(K):
         step(t, evs[k])
         if k in ck_steps:
+            # the pinned image is free once the previous write is on disk:
+            # wait for that here, so that the pack events hold the kernel only
+            h0 = time.perf_counter()
+            osr.ckpt_wait(ctx)
+            wait_s.append(time.perf_counter() - h0)
             a, b, c = pack_ev[k]
             a.record(main)
             osr.ckpt_pack(ctx, t, w, m, v, main_stream=main, side_stream=side)
@@ -422,8 +428,9 @@ def run_ours(args):
         },
         "checkpoint": {
             "bytes": 8 + 12 * n, "pack_ms": statistics.mean(pack_ms),
-            "d2h_ms": statistics.mean(d2h_ms),
+            "d2h_ms": statistics.mean(d2h_ms), "d2h_ms_each": d2h_ms,
             "d2h_GB/s": (8 + 12 * n) / (statistics.mean(d2h_ms) / 1e3) / 1e9,
+            "wait_prev_write_s_each": wait_s,
             "write_fsync_s": write_s, "write_GB/s": (8 + 12 * n) / write_s / 1e9,
             "dir": "temp dir under " + (args.ckpt_dir or tempfile.gettempdir()),
             "writer": "asynchronous thread, O_DIRECT, tmp + fsync + rename",
