@@ -108,6 +108,11 @@ class Oracle:
             c.c_int64, c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
             c.c_double, c.c_double, c.c_double, c.POINTER(c.c_double)]
         lib.oracle_adamw_clip_step_mixed.restype = c.c_int
+        lib.oracle_adamw_clip_step_masked.argtypes = [
+            _f32p, _f32p, _f32p, _f32p, c.c_int64, _i64p, _i64p, c.c_int32, _u8p,
+            c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double, c.c_double,
+            c.c_double, c.POINTER(c.c_double)]
+        lib.oracle_adamw_clip_step_masked.restype = c.c_int
         lib.oracle_adamw_at.argtypes = [
             _i64p, c.c_int64, _f32p, _f32p, _f32p, _f32p, c.c_double,
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
@@ -199,6 +204,26 @@ class Oracle:
         return st, norm.value
 
     # 16-bit formats: dtype 0 = float32, 1 = bfloat16, 2 = IEEE binary16
+    def adamw_clip_step_masked(self, w, g, m, v, offsets, numels, decay, t, lr, wd, clip,
+                               beta1=BETA1, beta2=BETA2, eps=EPS, raise_on_error=True):
+        """In-place step with a per-tensor decay flag (0: that tensor is
+        updated with wd = 0); the tensors must tile [0, n) in order."""
+        for a in (w, m, v):
+            _check_inplace(a)
+        g = _f32(g)
+        off = np.ascontiguousarray(offsets, dtype=np.int64)
+        num = np.ascontiguousarray(numels, dtype=np.int64)
+        dec = np.ascontiguousarray(np.asarray(decay) != 0, dtype=np.uint8)
+        if not (off.size == num.size == dec.size):
+            raise ValueError("offsets, numels and decay differ in length")
+        norm = ctypes.c_double()
+        st = self._lib.oracle_adamw_clip_step_masked(
+            w, g, m, v, w.size, off, num, off.size, dec, int(t), float(lr), float(wd),
+            float(clip), float(beta1), float(beta2), float(eps), ctypes.byref(norm))
+        if st not in (OK, ENONFINITE) or (st != OK and raise_on_error):
+            raise OracleError(st, "oracle_adamw_clip_step_masked")
+        return st, norm.value
+
     def decode16(self, h: int, dtype: int) -> float:
         return self._lib.oracle_decode16(int(h), int(dtype))
 

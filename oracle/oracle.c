@@ -329,6 +329,54 @@ int oracle_adamw_clip_step_mixed(float* w, const void* g, int32_t g_dtype, float
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------
+ * Per-group weight decay.  [T] "The Exact Targets of Clipping and AdamW":
+ * the lesson applies the decoupled decay to every parameter, normalisation
+ * gains and biases included, as a simple convention that it does not claim
+ * to be the best grouping.  The other grouping kept here: a flag per tensor
+ * of the offset table; a tensor whose flag is 0 is updated with wd = 0 (its
+ * old weight is multiplied by exactly 1), every other tensor with wd.  The
+ * norm and the clip factor stay global over all of g.  The tensors must
+ * tile [0, n) in order (offsets[k] + numels[k] == offsets[k + 1]).
+ * ---------------------------------------------------------------------- */
+int oracle_adamw_clip_step_masked(float* w, const float* g, float* m, float* v,
+                                  int64_t n, const int64_t* offsets,
+                                  const int64_t* numels, int32_t n_tensors,
+                                  const uint8_t* decay, int32_t t, double lr,
+                                  double wd, double clip, double beta1,
+                                  double beta2, double eps, double* norm_out)
+{
+    if (n < 0 || t < 1 || n_tensors < 0)
+        return OR_EINVAL;
+    int64_t next = 0;
+    for (int32_t k = 0; k < n_tensors; ++k) {
+        if (offsets[k] != next || numels[k] < 0)
+            return OR_EINVAL;
+        next = offsets[k] + numels[k];
+    }
+    if (next != n)
+        return OR_EINVAL;
+    double norm = oracle_global_norm(g, n);
+    if (norm_out)
+        *norm_out = norm;
+    if (!isfinite(norm))
+        return OR_ENONFINITE;
+    double s = oracle_clip_scale(norm, clip);
+    for (int32_t k = 0; k < n_tensors; ++k) {
+        double wd_k = decay[k] ? wd : 0.0;
+        for (int64_t i = offsets[k]; i < offsets[k] + numels[k]; ++i) {
+            oracle_terms r;
+            oracle_adamw_element((double)w[i], (double)g[i], (double)m[i],
+                                 (double)v[i], s, t, lr, wd_k, beta1, beta2,
+                                 eps, &r);
+            w[i] = (float)r.w;
+            m[i] = (float)r.m;
+            v[i] = (float)r.v;
+        }
+    }
+    return OR_OK;
+}
+
 /* The same update at chosen indices only, given the clip factor s (from a
  * full-vector norm computed separately).  Used to check outputs of a large
  * state one element at a time.  Results go to the *_out arrays. */

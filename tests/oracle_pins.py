@@ -178,6 +178,105 @@ def pin_decay_on_every_parameter(o, tmp):
         assert math.isclose(r["w"] - r["w_decayed"], -r["update"], rel_tol=1e-12)
 
 
+# --- per-group weight decay ---------------------------------------------------
+
+_MASK_SIZES = (5, 3, 8, 1, 13, 4, 7, 2)
+_MASK_FLAGS = (1, 0, 0, 1, 0, 1, 1, 0)
+
+
+def _mask_table():
+    num = np.array(_MASK_SIZES, np.int64)
+    off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
+    return off, num, int(num.sum())
+
+
+def pin_decay_mask_partition(o, tmp):
+    """A per-tensor decay flag splits the step: every element of a flagged
+    tensor is bit for bit the plain step with wd, every element of an exempt
+    one the plain step with wd = 0, and the norm (hence the clip) stays
+    global.  The flags are not shift-symmetric, so an index slip shows."""
+    off, num, n = _mask_table()
+    rng = np.random.default_rng(21)
+    w0 = rng.normal(0, 0.5, n).astype(np.float32)
+    g = rng.normal(0, 0.6, n).astype(np.float32)
+    m0 = rng.normal(0, 0.01, n).astype(np.float32)
+    v0 = np.abs(rng.normal(0, 1e-3, n)).astype(np.float32)
+    lr, wd = 0.05, 0.3
+    outs = []
+    for mode in ("mask", "wd", "zero"):
+        w, m, v = w0.copy(), m0.copy(), v0.copy()
+        if mode == "mask":
+            _, norm = o.adamw_clip_step_masked(w, g, m, v, off, num, _MASK_FLAGS, 3, lr, wd, 1.0)
+        else:
+            _, norm = o.adamw_clip_step(w, g, m, v, 3, lr, wd if mode == "wd" else 0.0, 1.0)
+        outs.append((w, m, v, norm))
+    (wm, mm, vm, nm), (wa, ma, va, na), (wb, mb, vb, nb) = outs
+    assert nm == na == nb and o.clip_scale(nm, 1.0) < 1.0
+    assert mm.tobytes() == ma.tobytes() and vm.tobytes() == va.tobytes()
+    for k, flag in enumerate(_MASK_FLAGS):
+        sl = slice(off[k], off[k] + num[k])
+        ref = wa if flag else wb
+        assert wm[sl].tobytes() == ref[sl].tobytes(), (k, flag)
+        other = wb if flag else wa
+        assert np.all(wm[sl] != other[sl]), (k, flag)  # wd changes every weight here
+
+
+def pin_decay_mask_closed_forms(o, tmp):
+    """Example 1 with its one tensor exempt: at t = 1, m_hat = g_hat and
+    sqrt(v_hat) = |g_hat|, so w = 2 - 0.1 * 0.5 / (0.5 + 1e-8) (no 1 - lr wd
+    factor).  With all flags set the masked step is the plain step bit for
+    bit.  A zero gradient leaves an exempt weight exactly as it was and
+    decays a flagged one by exactly float32(w (1 - lr wd))."""
+    inp, _, _ = read_golden("example1.txt")
+    w = np.array([inp["w"]], np.float32)
+    m = np.zeros(1, np.float32)
+    v = np.zeros(1, np.float32)
+    o.adamw_clip_step_masked(w, np.array([inp["g"]], np.float32), m, v, [0], [1], [0],
+                             1, inp["lr"], inp["wd"], inp["clip"])
+    want = 2.0 - 0.1 * 0.5 / (0.5 + 1e-8)
+    assert abs(float(w[0]) - want) <= 2.0 ** -22, (w[0], want)
+    assert abs(float(w[0]) - 1.898) > 1e-3  # the decayed value is not reached
+
+    off, num, n = _mask_table()
+    rng = np.random.default_rng(22)
+    w0 = rng.normal(0, 1.0, n).astype(np.float32)
+    g = rng.normal(0, 0.1, n).astype(np.float32)
+    wa, ma, va = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    wm, mm, vm = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    o.adamw_clip_step(wa, g, ma, va, 2, 1e-2, 0.1, 1.0)
+    o.adamw_clip_step_masked(wm, g, mm, vm, off, num, np.ones(len(num)), 2, 1e-2, 0.1, 1.0)
+    assert wa.tobytes() == wm.tobytes() and ma.tobytes() == mm.tobytes()
+
+    z = np.zeros(n, np.float32)
+    wz, mz, vz = w0.copy(), z.copy(), z.copy()
+    o.adamw_clip_step_masked(wz, z, mz, vz, off, num, _MASK_FLAGS, 1, 0.25, 0.5, 1.0)
+    for k, flag in enumerate(_MASK_FLAGS):
+        sl = slice(off[k], off[k] + num[k])
+        if flag:
+            want = (w0[sl].astype(np.float64) * (1.0 - 0.25 * 0.5)).astype(np.float32)
+            assert wz[sl].tobytes() == want.tobytes(), k
+        else:
+            assert wz[sl].tobytes() == w0[sl].tobytes(), k
+
+
+def pin_decay_mask_rejects_bad_table(o, tmp):
+    """The tensors must tile [0, n) in order: a gap, an overlap or a short
+    cover is refused and leaves the state untouched."""
+    n = 10
+    for off, num in (([0, 6], [5, 4]), ([0, 4], [5, 5]), ([0, 5], [5, 4])):
+        w = np.ones(n, np.float32)
+        m = np.zeros(n, np.float32)
+        v = np.zeros(n, np.float32)
+        try:
+            o.adamw_clip_step_masked(w, np.ones(n, np.float32), m, v, off, num, [1, 0],
+                                     1, 0.1, 0.1, 1.0)
+        except Exception:  # noqa: BLE001 - the refusal is the expected outcome
+            pass
+        else:
+            raise AssertionError(f"table {off} {num} accepted")
+        assert np.all(w == 1.0) and np.all(m == 0.0)
+
+
 # --- norm and clip -----------------------------------------------------------
 
 def pin_norm_pythagorean(o, tmp):

@@ -78,6 +78,14 @@ MUTANTS = {
                                 "double x = (double)g[i];\n        sumsq = sumsq + x * x;"),
     "scaled_update_unscaled": ("oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,",
                                "oracle_adamw_element((double)w[i], (double)g[i],"),
+    "mask_ignored": ("double wd_k = decay[k] ? wd : 0.0;", "double wd_k = wd;"),
+    "mask_inverted": ("double wd_k = decay[k] ? wd : 0.0;", "double wd_k = decay[k] ? 0.0 : wd;"),
+    "mask_shifted": ("double wd_k = decay[k] ? wd : 0.0;",
+                     "double wd_k = decay[k + 1 < n_tensors ? k + 1 : k] ? wd : 0.0;"),
+    "mask_skips_exempt_update": ("double wd_k = decay[k] ? wd : 0.0;",
+                                 "double wd_k = decay[k] ? wd : 0.0;\n        if (!decay[k]) continue;"),
+    "mask_range_short": ("i < offsets[k] + numels[k]; ++i)", "i + 1 < offsets[k] + numels[k]; ++i)"),
+    "mask_no_table_check": ("if (offsets[k] != next || numels[k] < 0)", "if (numels[k] < 0)"),
     "scaled_twice": ("double x = (double)g[i] * grad_scale;",
                      "double x = (double)g[i] * grad_scale * grad_scale;"),
 }
