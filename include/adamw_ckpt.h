@@ -255,6 +255,28 @@ ADAMW_API int grad_tensor_sumsq(adamw_ctx* ctx, const float* d_g, double* h_out,
 ADAMW_API int adamw_last_tensor_sumsq(adamw_ctx* ctx, double* h_out);
 
 /*
+ * Per-group weight decay ("Training as a Recoverable State Transition",
+ * section "The Exact Targets of Clipping and AdamW": the lesson decays every
+ * parameter, normalisation gains and biases included, and does not claim
+ * that this is the best grouping).  decay: one byte per tensor of the
+ * context's offset table (n_tensors must equal adamw_num_tensors); 0 exempts
+ * that tensor: every later step of this context updates its elements with
+ * wd = 0, i.e. its old weight is multiplied by exactly 1.  The norm and the
+ * clip stay global.  decay == NULL (n_tensors ignored), or all flags set,
+ * restores the default: decay on every parameter.
+ * Applies to adamw_clip_step, adamw_clip_step_ex, adamw_clip_step_mixed and
+ * the step graph (adamw_clip_step_noalloc, having no context, always decays
+ * everything).  The flags are configuration, not state: the checkpoint
+ * format has no place for them, so a resumed run sets them again.
+ * A setup call, not for the training loop: it waits for all work on the
+ * device, then copies one bit per parameter to the device (allocated by
+ * the first call that exempts a tensor, n / 8 bytes, freed with the
+ * context).  Errors: ADAMW_EINVAL (NULL ctx, n_tensors mismatch),
+ * ADAMW_ECUDA.
+ */
+ADAMW_API int adamw_set_decay_mask(adamw_ctx* ctx, const uint8_t* decay, int32_t n_tensors);
+
+/*
  * Waits for the last norm reduction launched on this context (by
  * grad_global_norm or adamw_clip_step) and reports it: *norm_out (may be
  * NULL) receives the norm of the (scaled) gradient in double, *scale_out

@@ -58,6 +58,7 @@ SIGNATURES = {
     "adamw_graph_destroy": (_c.c_int, [_vp]),
     "adamw_record_events": (_c.c_int, [_vp, _vp, _vp, _vp]),
     "adamw_set_launch_options": (_c.c_int, [_vp, _c.c_int32]),
+    "adamw_set_decay_mask": (_c.c_int, [_vp, _vp, _c.c_int32]),
     "adamw_clip_step_noalloc": (_c.c_int, [_vp, _vp, _vp, _vp, _c.c_int64, _c.c_int32,
                                            _c.c_double, _c.c_double, _c.c_double,
                                            _c.c_double, _c.c_double, _c.c_double, _vp, _vp]),
@@ -375,6 +376,18 @@ def adamw_clip_step_noalloc(w, g, m, v, t: int, lr: float, wd: float, clip: floa
 def adamw_set_launch_options(ctx: Context, flags: int = 0):
     _check(library().adamw_set_launch_options(ctx.handle, int(flags)),
            "adamw_set_launch_options")
+
+
+def adamw_set_decay_mask(ctx: Context, decay=None):
+    """Per-tensor decay flags (a sequence of bools, one per tensor of the
+    context's table; False exempts that tensor from weight decay).  None
+    restores decay on every parameter."""
+    if decay is None:
+        _check(library().adamw_set_decay_mask(ctx.handle, None, 0), "adamw_set_decay_mask")
+        return
+    flags = (_c.c_uint8 * len(decay))(*[1 if f else 0 for f in decay])
+    _check(library().adamw_set_decay_mask(ctx.handle, flags, len(decay)),
+           "adamw_set_decay_mask")
 
 
 def adamw_record_events(ctx: Context, ev_begin=None, ev_mid=None, ev_end=None):

@@ -88,6 +88,7 @@ void free_ctx(adamw_ctx* c)
         if (c->h_res) cudaFreeHost(c->h_res);
         if (c->d_image_alloc) cudaFree(c->d_image_alloc);
         if (c->h_image_alloc) cudaFreeHost(c->h_image_alloc);
+        if (c->d_decay_mask) cudaFree(c->d_decay_mask);
     }
     delete c;
 }
@@ -209,7 +210,21 @@ StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double w
     k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
     k.decay = float(1.0 - lr * wd);
     k.scale = 1.0f;
+    k.decay_mask = c->decay_mask_on ? c->d_decay_mask : nullptr;
     return k;
+}
+
+// Sets bits [lo, hi) of a bit array (bit e % 32 of word e / 32).
+void set_bit_range(uint32_t* words, int64_t lo, int64_t hi)
+{
+    while (lo < hi && (lo & 31)) {
+        words[lo >> 5] |= 1u << (lo & 31);
+        ++lo;
+    }
+    for (; lo + 32 <= hi; lo += 32)
+        words[lo >> 5] = 0xffffffffu;
+    for (; lo < hi; ++lo)
+        words[lo >> 5] |= 1u << (lo & 31);
 }
 
 }  // namespace osr
@@ -357,6 +372,43 @@ int adamw_set_hparams(adamw_ctx* ctx, double beta1, double beta2, double eps)
     ctx->beta1 = beta1;
     ctx->beta2 = beta2;
     ctx->eps = eps;
+    return ADAMW_OK;
+}
+
+int adamw_set_decay_mask(adamw_ctx* ctx, const uint8_t* decay, int32_t n_tensors)
+{
+    osr::clear_error();
+    if (!ctx)
+        return fail(ADAMW_EINVAL, "ctx is NULL");
+    bool all = true;
+    if (decay) {
+        if (n_tensors != int32_t(ctx->offsets.size()))
+            return fail(ADAMW_EINVAL, "n_tensors=%d, the context's table has %d tensors",
+                        n_tensors, int32_t(ctx->offsets.size()));
+        for (int32_t k = 0; k < n_tensors; ++k)
+            all = all && decay[k] != 0;
+    }
+    DeviceScope scope(ctx->device);
+    // no step of this context may still be reading the flags being replaced
+    CUDA_TRY(cudaDeviceSynchronize());
+    if (all) {  // decay everywhere: the kernels need no flags
+        ctx->decay_mask_on = false;
+        return ADAMW_OK;
+    }
+    const size_t words = size_t((ctx->n + 31) / 32);
+    std::vector<uint32_t> h(words, 0u);
+    for (int32_t k = 0; k < n_tensors; ++k)
+        if (decay[k])
+            osr::set_bit_range(h.data(), ctx->offsets[k], ctx->offsets[k] + ctx->numels[k]);
+    if (!ctx->d_decay_mask) {
+        cudaError_t e = cudaMalloc(&ctx->d_decay_mask, (words * 4 + 15) & ~size_t(15));
+        if (e != cudaSuccess) {
+            ctx->d_decay_mask = nullptr;
+            return cuda_fail(e, "cudaMalloc(decay flags)");
+        }
+    }
+    CUDA_TRY(cudaMemcpy(ctx->d_decay_mask, h.data(), words * 4, cudaMemcpyHostToDevice));
+    ctx->decay_mask_on = true;
     return ADAMW_OK;
 }
 

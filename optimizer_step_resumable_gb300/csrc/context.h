@@ -63,6 +63,10 @@ struct adamw_ctx {
     bool segs_launched = false;        // the last reduction also wrote segments
     cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
     bool pdl = true;  // launch the fused kernel as a programmatic dependent
+    // Per-tensor decay flags expanded to one bit per element (allocated by
+    // the first adamw_set_decay_mask that exempts a tensor).
+    uint32_t* d_decay_mask = nullptr;
+    bool decay_mask_on = false;
 
     // Checkpoint staging.  Device image at alloc + 8, so that its w region
     // (image + 8) starts on a 16-byte boundary for the pack kernel's vector

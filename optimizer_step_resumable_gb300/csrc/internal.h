@@ -41,6 +41,9 @@ struct StepScalars {
     float inv_sqrt_bc2;     // 1 / sqrt(1 - beta2^t)
     float decay;            // 1 - lr * wd
     float scale;            // gradient factor when no norm result is read
+    // Per-element decay flags (bit e % 32 of word e / 32 set: element e
+    // decays); NULL: every element decays.
+    const uint32_t* decay_mask;
 };
 
 // Tunables of the kernels (fixed at compile time; used in norm.cu, step.cu).

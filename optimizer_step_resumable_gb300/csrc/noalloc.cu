@@ -137,6 +137,7 @@ extern "C" int adamw_clip_step_noalloc(float* d_w, const float* d_g, float* d_m,
     k.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
     k.decay = float(1.0 - lr * wd);
     k.scale = 1.0f;  // unused: the factor comes from the norm result
+    k.decay_mask = nullptr;  // decay on every parameter
 
     int le = osr::launch_norm(d_g, n, clip, partials, counter, res, nullptr, stream);
     if (le != cudaSuccess)

@@ -31,26 +31,42 @@ namespace {
 //                                                     first, so g_hat^2 never
 //                                                     overflows on its own)
 //   denom = sqrt(v) / sqrt(1 - beta2^t) + eps        (one fma) = sqrt(v_hat)+eps
-//   w     = w (1 - lr wd) - (lr / (1 - beta1^t)) (m / denom)      (one fma)
+//   w     = w d - (lr / (1 - beta1^t)) (m / denom)   (one fma)
+// where d = 1 - lr wd, or exactly 1 for an element exempt from decay.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void adamw_elem(float& w, float g, float& m, float& v,
-                                           float s, const StepScalars& k)
+                                           float s, const StepScalars& k, float d)
 {
     const float gh = __fmul_rn(g, s);
     m = __fmaf_rn(k.beta1, m, __fmul_rn(k.omb1, gh));
     v = __fmaf_rn(k.beta2, v, __fmul_rn(__fmul_rn(k.omb2, gh), gh));
     const float denom = __fmaf_rn(__fsqrt_rn(v), k.inv_sqrt_bc2, k.eps);
     const float upd = __fmul_rn(k.step_size, __fdiv_rn(m, denom));
-    w = __fmaf_rn(w, k.decay, -upd);
+    w = __fmaf_rn(w, d, -upd);
 }
 
+// bits: the decay flags of the four elements (bit j set: element j decays).
 __device__ __forceinline__ void adamw4(float4& w, float4 g, float4& m, float4& v,
-                                       float s, const StepScalars& k)
+                                       float s, const StepScalars& k, uint32_t bits)
 {
-    adamw_elem(w.x, g.x, m.x, v.x, s, k);
-    adamw_elem(w.y, g.y, m.y, v.y, s, k);
-    adamw_elem(w.z, g.z, m.z, v.z, s, k);
-    adamw_elem(w.w, g.w, m.w, v.w, s, k);
+    adamw_elem(w.x, g.x, m.x, v.x, s, k, (bits & 1u) ? k.decay : 1.0f);
+    adamw_elem(w.y, g.y, m.y, v.y, s, k, (bits & 2u) ? k.decay : 1.0f);
+    adamw_elem(w.z, g.z, m.z, v.z, s, k, (bits & 4u) ? k.decay : 1.0f);
+    adamw_elem(w.w, g.w, m.w, v.w, s, k, (bits & 8u) ? k.decay : 1.0f);
+}
+
+// Per-group weight decay: element e decays when bit e % 32 of word e / 32 of
+// the mask is set; no mask (NULL) means every element decays.  The flags of
+// the float4 at float4 index i are the nibble (i % 8) of word i / 8.
+__device__ __forceinline__ uint32_t decay_nibble(const uint32_t* __restrict__ mask, int64_t i)
+{
+    return mask ? (__ldg(mask + (i >> 3)) >> ((int(i) & 7) << 2)) & 0xFu : 0xFu;
+}
+
+__device__ __forceinline__ float decay_one(const uint32_t* __restrict__ mask, int64_t e,
+                                           const StepScalars& k)
+{
+    return (!mask || ((__ldg(mask + (e >> 5)) >> (int(e) & 31)) & 1u)) ? k.decay : 1.0f;
 }
 
 constexpr int kStepThreads = 256;
@@ -64,13 +80,15 @@ constexpr int kStepVec = 2;  // float4 of each array per thread per chunk
 // type (float, bfloat16, binary16; widened exactly).  kZero also writes 0
 // into g after reading it ("zero_grads" for the next accumulation).  WL, if
 // not void, is the type of a 16-bit copy of the new weights written to w_lp
-// (rounded to nearest even) for the next forward pass.
+// (rounded to nearest even) for the next forward pass.  k.decay_mask (may
+// be NULL) holds one decay flag per element, as decay_nibble reads it.
 template <bool kVec, bool kZero, typename G, typename WL>
 __global__ void __launch_bounds__(kStepThreads)
     k_clip_adamw(float* __restrict__ w, const G* __restrict__ g,
                  float* __restrict__ m, float* __restrict__ v, int64_t n,
                  StepScalars k, const NormResult* __restrict__ res, WL* __restrict__ w_lp)
 {
+    const uint32_t* __restrict__ decay_mask = k.decay_mask;
     constexpr bool kCopy = !std::is_void<WL>::value;
     // When launched right behind the norm kernel with programmatic
     // serialization, this grid may start while that kernel still runs: warm
@@ -111,6 +129,7 @@ __global__ void __launch_bounds__(kStepThreads)
         for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
             const int64_t i0 = c * chunk + threadIdx.x;
             float4 W[kStepVec], G4[kStepVec], M[kStepVec], V[kStepVec];
+            uint32_t D[kStepVec];
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j) {
                 const int64_t i = i0 + j * kStepThreads;
@@ -118,10 +137,11 @@ __global__ void __launch_bounds__(kStepThreads)
                 G4[j] = detail::load4_cs<G>(g + (i << 2));
                 M[j] = __ldcs(m4 + i);
                 V[j] = __ldcs(v4 + i);
+                D[j] = decay_nibble(decay_mask, i);
             }
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j)
-                adamw4(W[j], G4[j], M[j], V[j], s, k);
+                adamw4(W[j], G4[j], M[j], V[j], s, k, D[j]);
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j) {
                 const int64_t i = i0 + j * kStepThreads;
@@ -137,7 +157,7 @@ __global__ void __launch_bounds__(kStepThreads)
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
             float4 W = __ldcs(w4 + i), G4 = detail::load4_cs<G>(g + (i << 2)),
                    M = __ldcs(m4 + i), V = __ldcs(v4 + i);
-            adamw4(W, G4, M, V, s, k);
+            adamw4(W, G4, M, V, s, k, decay_nibble(decay_mask, i));
             __stcs(w4 + i, W);
             __stcs(m4 + i, M);
             __stcs(v4 + i, V);
@@ -149,7 +169,7 @@ __global__ void __launch_bounds__(kStepThreads)
         if (gtid < (n & 3)) {
             const int64_t e = (n4 << 2) + gtid;
             float W = w[e], M = m[e], V = v[e];
-            adamw_elem(W, detail::load1(g + e), M, V, s, k);
+            adamw_elem(W, detail::load1(g + e), M, V, s, k, decay_one(decay_mask, e, k));
             w[e] = W;
             m[e] = M;
             v[e] = V;
@@ -161,7 +181,7 @@ __global__ void __launch_bounds__(kStepThreads)
     } else {  // float32 state at 4-byte boundaries, float32 gradient, no copy
         for (int64_t e = gtid; e < n; e += stride) {
             float W = __ldcs(w + e), M = __ldcs(m + e), V = __ldcs(v + e);
-            adamw_elem(W, __ldcs(g + e), M, V, s, k);
+            adamw_elem(W, __ldcs(g + e), M, V, s, k, decay_one(decay_mask, e, k));
             __stcs(w + e, W);
             __stcs(m + e, M);
             __stcs(v + e, V);

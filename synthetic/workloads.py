@@ -43,6 +43,13 @@ def gpt_110m_tensors():
     return out
 
 
+def decay_flags_matrices_only(tensors):
+    """The common alternative grouping: weight decay on matrices and
+    embeddings, none on biases and normalisation gains/shifts (every 1-D
+    tensor of the list).  One flag per tensor, in table order."""
+    return [0 if (".b_" in name or "ln" in name) else 1 for name, _ in tensors]
+
+
 def offset_table(tensors):
     """(offsets, numels) of a contiguous flat layout, in the given order."""
     offsets, numels, off = [], [], 0
