@@ -265,8 +265,10 @@ ADAMW_API int adamw_last_tensor_sumsq(adamw_ctx* ctx, double* h_out);
  * clip stay global.  decay == NULL (n_tensors ignored), or all flags set,
  * restores the default: decay on every parameter.
  * Applies to adamw_clip_step, adamw_clip_step_ex, adamw_clip_step_mixed and
- * the step graph (adamw_clip_step_noalloc, having no context, always decays
- * everything).  The flags are configuration, not state: the checkpoint
+ * the step graph (a graph made before the flags were set or cleared is
+ * rebuilt by its next adamw_graph_step; adamw_clip_step_noalloc, having no
+ * context, always decays everything).  Without flags the fused kernel is
+ * compiled without the flag reads.  The flags are configuration, not state: the checkpoint
  * format has no place for them, so a resumed run sets them again.
  * A setup call, not for the training loop: it waits for all work on the
  * device, then copies one bit per parameter to the device (allocated by

@@ -88,6 +88,7 @@ struct adamw_ctx {
     const float* graph_g = nullptr;
     float* graph_m = nullptr;
     float* graph_v = nullptr;
+    bool graph_mask = false;  // the graph's fused node reads decay flags
 
     // Checkpoint writing: options and the writer thread.
     int32_t keep = 0;                   // rotation: newest files kept (0 = all)

@@ -56,6 +56,35 @@ int cuda_fail(cudaError_t e, const char* what)
     return fail(ADAMW_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Builds and instantiates the two-node graph over the context's graph_*
+// pointers.  The fused node's kernel variant depends on whether decay flags
+// are set (an instantiated node cannot change its function), so the graph
+// remembers that and is rebuilt when it changes.
+int graph_build(adamw_ctx* ctx)
+{
+    NormNodeArgs na;
+    AdamwNodeArgs aa;
+    cudaKernelNodeParams np{}, ap{};
+    fill_args(ctx, INFINITY, make_step_scalars(ctx, 1, 0.0, 0.0), &na, &aa, &np, &ap);
+    cudaError_t e;
+    int rc = ADAMW_OK;
+    if ((e = cudaGraphCreate(&ctx->graph, 0)) != cudaSuccess)
+        rc = cuda_fail(e, "cudaGraphCreate");
+    else if ((e = cudaGraphAddKernelNode(&ctx->graph_norm, ctx->graph, nullptr, 0, &np)) !=
+             cudaSuccess)
+        rc = cuda_fail(e, "cudaGraphAddKernelNode(norm)");
+    else if ((e = cudaGraphAddKernelNode(&ctx->graph_step, ctx->graph, &ctx->graph_norm, 1,
+                                         &ap)) != cudaSuccess)
+        rc = cuda_fail(e, "cudaGraphAddKernelNode(step)");
+    else if ((e = cudaGraphInstantiate(&ctx->graph_exec, ctx->graph, 0)) != cudaSuccess)
+        rc = cuda_fail(e, "cudaGraphInstantiate");
+    if (rc != ADAMW_OK)
+        graph_release(ctx);
+    else
+        ctx->graph_mask = ctx->decay_mask_on;
+    return rc;
+}
+
 }  // namespace
 }  // namespace osr
 
@@ -80,24 +109,7 @@ int adamw_graph_create(adamw_ctx* ctx, float* d_w, const float* d_g, float* d_m,
     ctx->graph_g = d_g;
     ctx->graph_m = d_m;
     ctx->graph_v = d_v;
-    osr::NormNodeArgs na;
-    osr::AdamwNodeArgs aa;
-    cudaKernelNodeParams np{}, ap{};
-    osr::fill_args(ctx, INFINITY, osr::make_step_scalars(ctx, 1, 0.0, 0.0), &na, &aa, &np, &ap);
-    cudaError_t e;
-    int rc = ADAMW_OK;
-    if ((e = cudaGraphCreate(&ctx->graph, 0)) != cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphCreate");
-    else if ((e = cudaGraphAddKernelNode(&ctx->graph_norm, ctx->graph, nullptr, 0, &np)) !=
-             cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphAddKernelNode(norm)");
-    else if ((e = cudaGraphAddKernelNode(&ctx->graph_step, ctx->graph, &ctx->graph_norm, 1,
-                                         &ap)) != cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphAddKernelNode(step)");
-    else if ((e = cudaGraphInstantiate(&ctx->graph_exec, ctx->graph, 0)) != cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphInstantiate");
-    if (rc != ADAMW_OK)
-        osr::graph_release(ctx);
+    const int rc = osr::graph_build(ctx);
     if (prev >= 0 && prev != ctx->device)
         cudaSetDevice(prev);
     return rc;
@@ -119,13 +131,31 @@ int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd, double cli
     cudaGetDevice(&prev);
     if (prev != ctx->device)
         cudaSetDevice(ctx->device);
+    int rc = ADAMW_OK;
+    if (ctx->graph_mask != ctx->decay_mask_on) {
+        // decay flags set or cleared since the graph was built
+        float* w = ctx->graph_w;
+        const float* g = ctx->graph_g;
+        float* m = ctx->graph_m;
+        float* v = ctx->graph_v;
+        osr::graph_release(ctx);
+        ctx->graph_w = w;
+        ctx->graph_g = g;
+        ctx->graph_m = m;
+        ctx->graph_v = v;
+        rc = osr::graph_build(ctx);
+        if (rc != ADAMW_OK) {
+            if (prev >= 0 && prev != ctx->device)
+                cudaSetDevice(prev);
+            return rc;
+        }
+    }
     osr::NormNodeArgs na;
     osr::AdamwNodeArgs aa;
     cudaKernelNodeParams np{}, ap{};
     osr::fill_args(ctx, clip, osr::make_step_scalars(ctx, t, lr, wd), &na, &aa, &np, &ap);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    int rc = ADAMW_OK;
     if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_norm, &np)) !=
         cudaSuccess)
         rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(norm)");

@@ -56,17 +56,26 @@ __device__ __forceinline__ void adamw4(float4& w, float4 g, float4& m, float4& v
 }
 
 // Per-group weight decay: element e decays when bit e % 32 of word e / 32 of
-// the mask is set; no mask (NULL) means every element decays.  The flags of
-// the float4 at float4 index i are the nibble (i % 8) of word i / 8.
+// the mask is set.  The flags of the float4 at float4 index i are the nibble
+// (i % 8) of word i / 8.  Without kMask every element decays, and the
+// selects fold away at compile time.
+template <bool kMask>
 __device__ __forceinline__ uint32_t decay_nibble(const uint32_t* __restrict__ mask, int64_t i)
 {
-    return mask ? (__ldg(mask + (i >> 3)) >> ((int(i) & 7) << 2)) & 0xFu : 0xFu;
+    if constexpr (kMask)
+        return (__ldg(mask + (i >> 3)) >> ((int(i) & 7) << 2)) & 0xFu;
+    else
+        return 0xFu;
 }
 
+template <bool kMask>
 __device__ __forceinline__ float decay_one(const uint32_t* __restrict__ mask, int64_t e,
                                            const StepScalars& k)
 {
-    return (!mask || ((__ldg(mask + (e >> 5)) >> (int(e) & 31)) & 1u)) ? k.decay : 1.0f;
+    if constexpr (kMask)
+        return ((__ldg(mask + (e >> 5)) >> (int(e) & 31)) & 1u) ? k.decay : 1.0f;
+    else
+        return k.decay;
 }
 
 constexpr int kStepThreads = 256;
@@ -80,9 +89,9 @@ constexpr int kStepVec = 2;  // float4 of each array per thread per chunk
 // type (float, bfloat16, binary16; widened exactly).  kZero also writes 0
 // into g after reading it ("zero_grads" for the next accumulation).  WL, if
 // not void, is the type of a 16-bit copy of the new weights written to w_lp
-// (rounded to nearest even) for the next forward pass.  k.decay_mask (may
-// be NULL) holds one decay flag per element, as decay_nibble reads it.
-template <bool kVec, bool kZero, typename G, typename WL>
+// (rounded to nearest even) for the next forward pass.  kMask: k.decay_mask
+// holds one decay flag per element, as decay_nibble reads it.
+template <bool kVec, bool kZero, typename G, typename WL, bool kMask>
 __global__ void __launch_bounds__(kStepThreads)
     k_clip_adamw(float* __restrict__ w, const G* __restrict__ g,
                  float* __restrict__ m, float* __restrict__ v, int64_t n,
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(kStepThreads)
                 G4[j] = detail::load4_cs<G>(g + (i << 2));
                 M[j] = __ldcs(m4 + i);
                 V[j] = __ldcs(v4 + i);
-                D[j] = decay_nibble(decay_mask, i);
+                D[j] = decay_nibble<kMask>(decay_mask, i);
             }
 #pragma unroll
             for (int j = 0; j < kStepVec; ++j)
@@ -157,7 +166,7 @@ __global__ void __launch_bounds__(kStepThreads)
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
             float4 W = __ldcs(w4 + i), G4 = detail::load4_cs<G>(g + (i << 2)),
                    M = __ldcs(m4 + i), V = __ldcs(v4 + i);
-            adamw4(W, G4, M, V, s, k, decay_nibble(decay_mask, i));
+            adamw4(W, G4, M, V, s, k, decay_nibble<kMask>(decay_mask, i));
             __stcs(w4 + i, W);
             __stcs(m4 + i, M);
             __stcs(v4 + i, V);
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kStepThreads)
         if (gtid < (n & 3)) {
             const int64_t e = (n4 << 2) + gtid;
             float W = w[e], M = m[e], V = v[e];
-            adamw_elem(W, detail::load1(g + e), M, V, s, k, decay_one(decay_mask, e, k));
+            adamw_elem(W, detail::load1(g + e), M, V, s, k, decay_one<kMask>(decay_mask, e, k));
             w[e] = W;
             m[e] = M;
             v[e] = V;
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(kStepThreads)
     } else {  // float32 state at 4-byte boundaries, float32 gradient, no copy
         for (int64_t e = gtid; e < n; e += stride) {
             float W = __ldcs(w + e), M = __ldcs(m + e), V = __ldcs(v + e);
-            adamw_elem(W, __ldcs(g + e), M, V, s, k, decay_one(decay_mask, e, k));
+            adamw_elem(W, __ldcs(g + e), M, V, s, k, decay_one<kMask>(decay_mask, e, k));
             __stcs(w + e, W);
             __stcs(m + e, M);
             __stcs(v + e, V);
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(kStepThreads)
 // Launches the fused kernel; with `programmatic`, as a programmatic
 // dependent of the kernel before it in the stream (that kernel must be the
 // norm reduction, whose blocks release it early).
-template <bool kVec, bool kZero, typename G, typename WL>
+template <bool kVec, bool kZero, typename G, typename WL, bool kMask>
 void launch_step(int blocks, cudaStream_t s, bool programmatic, float* w, const void* g,
                  float* m, float* v, int64_t n, const StepScalars& k, const NormResult* d_res,
                  void* w_lp)
@@ -210,36 +219,60 @@ void launch_step(int blocks, cudaStream_t s, bool programmatic, float* w, const 
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
     // status: cudaGetLastError in the caller
-    cudaLaunchKernelEx(&cfg, &k_clip_adamw<kVec, kZero, G, WL>, w, static_cast<const G*>(g), m,
-                       v, n, k, d_res, static_cast<WL*>(w_lp));
+    cudaLaunchKernelEx(&cfg, &k_clip_adamw<kVec, kZero, G, WL, kMask>, w,
+                       static_cast<const G*>(g), m, v, n, k, d_res, static_cast<WL*>(w_lp));
 }
 
-template <bool kZero, typename G>
+template <bool kZero, typename G, bool kMask>
 void launch_vec(int blocks, cudaStream_t s, bool pdl, float* w, const void* g, float* m,
                 float* v, int64_t n, const StepScalars& k, const NormResult* d_res, void* w_lp,
                 int32_t w_lp_dtype)
 {
     if (!w_lp)
-        launch_step<true, kZero, G, void>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp);
+        launch_step<true, kZero, G, void, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp);
     else if (w_lp_dtype == kDtypeF16)
-        launch_step<true, kZero, G, __half>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp);
-    else
-        launch_step<true, kZero, G, __nv_bfloat16>(blocks, s, pdl, w, g, m, v, n, k, d_res,
+        launch_step<true, kZero, G, __half, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res,
                                                    w_lp);
+    else
+        launch_step<true, kZero, G, __nv_bfloat16, kMask>(blocks, s, pdl, w, g, m, v, n, k,
+                                                          d_res, w_lp);
 }
 
-template <bool kZero>
+template <bool kZero, bool kMask>
 void launch_vec_any(int32_t g_dtype, int blocks, cudaStream_t s, bool pdl, float* w,
                     const void* g, float* m, float* v, int64_t n, const StepScalars& k,
                     const NormResult* d_res, void* w_lp, int32_t w_lp_dtype)
 {
     if (g_dtype == kDtypeBF16)
-        launch_vec<kZero, __nv_bfloat16>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
-                                         w_lp_dtype);
+        launch_vec<kZero, __nv_bfloat16, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
+                                                w_lp_dtype);
     else if (g_dtype == kDtypeF16)
-        launch_vec<kZero, __half>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp, w_lp_dtype);
+        launch_vec<kZero, __half, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
+                                         w_lp_dtype);
     else
-        launch_vec<kZero, float>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp, w_lp_dtype);
+        launch_vec<kZero, float, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
+                                        w_lp_dtype);
+}
+
+template <bool kMask>
+void launch_any(bool vec, bool zero_grad, int32_t g_dtype, int blocks, cudaStream_t s,
+                bool pdl, float* w, const void* g, float* m, float* v, int64_t n,
+                const StepScalars& k, const NormResult* d_res, void* w_lp, int32_t w_lp_dtype)
+{
+    if (vec) {
+        if (zero_grad)
+            launch_vec_any<true, kMask>(g_dtype, blocks, s, pdl, w, g, m, v, n, k, d_res, w_lp,
+                                        w_lp_dtype);
+        else
+            launch_vec_any<false, kMask>(g_dtype, blocks, s, pdl, w, g, m, v, n, k, d_res,
+                                         w_lp, w_lp_dtype);
+    } else if (zero_grad) {
+        launch_step<false, true, float, void, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res,
+                                                     nullptr);
+    } else {
+        launch_step<false, false, float, void, kMask>(blocks, s, pdl, w, g, m, v, n, k, d_res,
+                                                      nullptr);
+    }
 }
 
 }  // namespace
@@ -249,11 +282,11 @@ int query_step_caps(int sm_count, KernelCaps* caps)
     // the other variants have the same shape and the same register budget
     cudaError_t err = cudaSuccess;
     caps->step_vec = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<true, false, float, void>), kStepThreads,
-        sm_count, &err);
+        reinterpret_cast<const void*>(&k_clip_adamw<true, false, float, void, false>),
+        kStepThreads, sm_count, &err);
     caps->step_scalar = detail::resident_blocks(
-        reinterpret_cast<const void*>(&k_clip_adamw<false, false, float, void>), kStepThreads,
-        sm_count, &err);
+        reinterpret_cast<const void*>(&k_clip_adamw<false, false, float, void, false>),
+        kStepThreads, sm_count, &err);
     return int(err);
 }
 
@@ -269,27 +302,16 @@ int launch_adamw(float* w, const void* g, float* m, float* v, int64_t n,
                      (!w_lp || detail::aligned8(w_lp));
     if (!vec && !plain)
         return int(cudaErrorMisalignedAddress);  // callers refuse this before launching
-    if (vec) {
-        const int cap = caps.step_vec;
-        const int64_t want = detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec);
-        const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        if (zero_grad)
-            launch_vec_any<true>(g_dtype, blocks, s, programmatic, w, g, m, v, n, k, d_res, w_lp,
-                                 w_lp_dtype);
-        else
-            launch_vec_any<false>(g_dtype, blocks, s, programmatic, w, g, m, v, n, k, d_res,
-                                  w_lp, w_lp_dtype);
-    } else {
-        const int cap = caps.step_scalar;
-        const int64_t want = detail::ceil_div(n, kStepThreads);
-        const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        if (zero_grad)
-            launch_step<false, true, float, void>(blocks, s, programmatic, w, g, m, v, n, k,
-                                                  d_res, nullptr);
-        else
-            launch_step<false, false, float, void>(blocks, s, programmatic, w, g, m, v, n, k,
-                                                   d_res, nullptr);
-    }
+    const int cap = vec ? caps.step_vec : caps.step_scalar;
+    const int64_t want = vec ? detail::ceil_div(n >> 2, int64_t(kStepThreads) * kStepVec)
+                             : detail::ceil_div(n, kStepThreads);
+    const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
+    if (k.decay_mask)
+        launch_any<true>(vec, zero_grad, g_dtype, blocks, s, programmatic, w, g, m, v, n, k,
+                         d_res, w_lp, w_lp_dtype);
+    else
+        launch_any<false>(vec, zero_grad, g_dtype, blocks, s, programmatic, w, g, m, v, n, k,
+                          d_res, w_lp, w_lp_dtype);
     return int(cudaGetLastError());
 }
 
@@ -308,12 +330,15 @@ int adamw_node_params(AdamwNodeArgs* a, const KernelCaps& caps, cudaKernelNodePa
                      detail::aligned16(a->m) && detail::aligned16(a->v);
     int64_t want;
     int cap;
+    const bool mask = a->k.decay_mask != nullptr;
     if (vec) {
-        p->func = reinterpret_cast<void*>(&k_clip_adamw<true, false, float, void>);
+        p->func = mask ? reinterpret_cast<void*>(&k_clip_adamw<true, false, float, void, true>)
+                       : reinterpret_cast<void*>(&k_clip_adamw<true, false, float, void, false>);
         want = detail::ceil_div(a->n >> 2, int64_t(kStepThreads) * kStepVec);
         cap = caps.step_vec;
     } else {
-        p->func = reinterpret_cast<void*>(&k_clip_adamw<false, false, float, void>);
+        p->func = mask ? reinterpret_cast<void*>(&k_clip_adamw<false, false, float, void, true>)
+                       : reinterpret_cast<void*>(&k_clip_adamw<false, false, float, void, false>);
         want = detail::ceil_div(a->n, kStepThreads);
         cap = caps.step_scalar;
     }

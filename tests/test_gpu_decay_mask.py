@@ -245,19 +245,23 @@ def test_bf16_gradient_path(dev, oracle):
 
 
 def test_graph_step_applies_the_flags(dev):
-    """The step graph reads the same flags: bit for bit the plain step."""
+    """The step graph reads the same flags, and setting or clearing them
+    after the graph was made takes effect at the next graph step: bit for
+    bit the plain steps through the same sequence."""
     sizes, flags = TABLES["big_ragged"]
     off, num = table(sizes)
     n = int(num.sum())
     hw, hg, hm, hv = inputs(n)
+    plan = {1: None, 2: flags, 3: None, 4: None, 5: [1 - f for f in flags], 6: None}
     outs = []
     for use_graph in (False, True):
         w, g, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv))
         with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
-            osr.adamw_set_decay_mask(ctx, flags)
             if use_graph:
                 osr.adamw_graph_create(ctx, w, g, m, v)
-            for t in (1, 2, 3):
+            for t in range(1, 7):
+                if t in (2, 4, 5):
+                    osr.adamw_set_decay_mask(ctx, plan[t])
                 if use_graph:
                     osr.adamw_graph_step(ctx, t, LR, WD, CLIP)
                 else:
