@@ -173,9 +173,14 @@ def max_over_ranks(x, world):
 # ---------------------------------------------------------------------------
 class OracleTimer:
     """The oracle's full step (norm, clip, AdamW) on the first S parameters
-    of the workload; single thread, inputs prepared once."""
+    of the workload, inputs prepared once.  With threads > 1 the sample is
+    cut into one contiguous slice per thread: each thread sums its slice's
+    squares (the oracle's sumsq), the sums are added in slice order, the
+    oracle's clip factor of the total is taken, and each thread updates its
+    slice with it (the oracle's update over a range).  The oracle's C calls
+    release the GIL, so the threads run on separate cores."""
 
-    def __init__(self, wl, sample=1 << 21):
+    def __init__(self, wl, sample=1 << 21, threads=1):
         import numpy as np
 
         import oracle
@@ -183,6 +188,12 @@ class OracleTimer:
         self.o = oracle.load()
         self.wl = wl
         self.S = S = min(wl.n, sample)
+        self.threads = max(1, min(threads, S))
+        self.bounds = [S * i // self.threads for i in range(self.threads + 1)]
+        self.pool = None
+        if self.threads > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            self.pool = ThreadPoolExecutor(self.threads)
         self.w = synthetic.weights(wl.seed, n=S)
         self.g = synthetic.grads(wl.seed, 1, wl.grad_sigma, n=S, outlier_frac=wl.outlier_frac,
                                  outlier_mult=wl.outlier_mult)
@@ -192,12 +203,26 @@ class OracleTimer:
         self.total_steps = 0
         self.total_s = 0.0
 
+    def step(self):
+        wl = self.wl
+        if self.pool is None:
+            self.o.adamw_clip_step(self.w, self.g, self.m, self.v, self.t, wl.lr, wl.wd, wl.clip)
+            return
+        b, T = self.bounds, self.threads
+        parts = list(self.pool.map(lambda i: self.o.sumsq(self.g[b[i]:b[i + 1]]), range(T)))
+        total = 0.0
+        for p in parts:  # slice order
+            total += p
+        s = self.o.clip_scale(math.sqrt(total), wl.clip)
+        list(self.pool.map(lambda i: self.o.adamw_update_range(
+            self.w, self.g, self.m, self.v, b[i], b[i + 1], s, self.t, wl.lr, wl.wd), range(T)))
+
     def run(self, seconds):
         """params/s over repeated steps lasting at least `seconds`."""
-        wl, reps = self.wl, 0
+        reps = 0
         t0 = time.perf_counter()
         while True:
-            self.o.adamw_clip_step(self.w, self.g, self.m, self.v, self.t, wl.lr, wl.wd, wl.clip)
+            self.step()
             reps += 1
             self.t += 1
             el = time.perf_counter() - t0
@@ -208,15 +233,37 @@ class OracleTimer:
         return self.S * reps / el
 
     def describe(self, value):
-        return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        how = ("single thread" if self.threads == 1 else
+               f"{self.threads} threads, one contiguous slice each, slice sums of squares "
+               f"added in slice order")
+        return {"value": value, "unit": UNIT, "cores": self.threads, "kind": "oracle",
                 "sample": f"oracle clip+AdamW step (norm, clip, update; double intermediates) "
                           f"on the first {self.S} parameters of {self.wl.name}, "
-                          f"{self.total_steps} steps in {self.total_s:.1f} s, single thread"}
+                          f"{self.total_steps} steps in {self.total_s:.1f} s, {how}"}
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def time_oracle(wl, seconds):
-    timer = OracleTimer(wl)
-    return timer.describe(timer.run(seconds))
+    """All host cores (the reported baseline) and, for context, one core."""
+    cores = host_cores()
+    timer = OracleTimer(wl, sample=1 << 24, threads=cores)
+    timer.run(min(1.0, seconds / 10))  # warm-up: first touch of the arrays
+    timer.total_steps, timer.total_s = 0, 0.0
+    out = timer.describe(timer.run(seconds * 2 / 3))
+    timer.close()
+    single = OracleTimer(wl)
+    out["single_thread"] = single.describe(single.run(seconds / 3))
+    return out
 
 
 def run_reference(args):
@@ -225,7 +272,7 @@ def run_reference(args):
         return 0
     wl = workload(args.workload)
     per_step = max(0.25, min(args.cpu_seconds, 90.0 / max(1, args.steps + args.warmup)))
-    timer = OracleTimer(wl)
+    timer = OracleTimer(wl, sample=1 << 24, threads=host_cores())
     for _ in range(args.warmup):
         timer.run(per_step / 4)
     timer.total_steps, timer.total_s = 0, 0.0
@@ -240,6 +287,7 @@ def run_reference(args):
         "cpu_baseline": timer.describe(value),
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    timer.close()
     print(json.dumps(line), flush=True)
     return 0
 

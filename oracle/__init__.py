@@ -113,6 +113,10 @@ class Oracle:
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double, c.c_double,
             c.c_double, c.POINTER(c.c_double)]
         lib.oracle_adamw_clip_step_masked.restype = c.c_int
+        lib.oracle_adamw_update_range.argtypes = [
+            _f32p, _f32p, _f32p, _f32p, c.c_int64, c.c_int64, c.c_double, c.c_int32,
+            c.c_double, c.c_double, c.c_double, c.c_double, c.c_double]
+        lib.oracle_adamw_update_range.restype = c.c_int
         lib.oracle_adamw_at.argtypes = [
             _i64p, c.c_int64, _f32p, _f32p, _f32p, _f32p, c.c_double,
             c.c_int32, c.c_double, c.c_double, c.c_double, c.c_double,
@@ -204,6 +208,22 @@ class Oracle:
         return st, norm.value
 
     # 16-bit formats: dtype 0 = float32, 1 = bfloat16, 2 = IEEE binary16
+    def adamw_update_range(self, w, g, m, v, lo, hi, s, t, lr, wd, beta1=BETA1, beta2=BETA2,
+                           eps=EPS):
+        """In-place update of elements [lo, hi) with the given clip factor s
+        (of the whole gradient).  The C call releases the GIL, so threads can
+        run disjoint ranges at once."""
+        for a in (w, m, v):
+            _check_inplace(a)
+        g = _f32(g)
+        if not (0 <= lo <= hi <= w.size) or not (g.size == m.size == v.size == w.size):
+            raise ValueError("range outside the arrays")
+        st = self._lib.oracle_adamw_update_range(w, g, m, v, int(lo), int(hi), float(s), int(t),
+                                                 float(lr), float(wd), float(beta1),
+                                                 float(beta2), float(eps))
+        if st != OK:
+            raise OracleError(st, "oracle_adamw_update_range")
+
     def adamw_clip_step_masked(self, w, g, m, v, offsets, numels, decay, t, lr, wd, clip,
                                beta1=BETA1, beta2=BETA2, eps=EPS, raise_on_error=True):
         """In-place step with a per-tensor decay flag (0: that tensor is

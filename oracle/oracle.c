@@ -329,6 +329,28 @@ int oracle_adamw_clip_step_mixed(float* w, const void* g, int32_t g_dtype, float
     return OR_OK;
 }
 
+/* The update half of the step over the index range [lo, hi) only, in place,
+ * given the clip factor s of the whole gradient: the same per-element
+ * definition as oracle_adamw_clip_step's loop.  Used to run the oracle on
+ * several host threads (each a disjoint range) for the CPU baseline. */
+int oracle_adamw_update_range(float* w, const float* g, float* m, float* v,
+                              int64_t lo, int64_t hi, double s, int32_t t,
+                              double lr, double wd, double beta1, double beta2,
+                              double eps)
+{
+    if (lo < 0 || hi < lo || t < 1)
+        return OR_EINVAL;
+    for (int64_t j = lo; j < hi; ++j) {
+        oracle_terms r;
+        oracle_adamw_element((double)w[j], (double)g[j], (double)m[j],
+                             (double)v[j], s, t, lr, wd, beta1, beta2, eps, &r);
+        w[j] = (float)r.w;
+        m[j] = (float)r.m;
+        v[j] = (float)r.v;
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------
  * Per-group weight decay.  [T] "The Exact Targets of Clipping and AdamW":
  * the lesson applies the decoupled decay to every parameter, normalisation

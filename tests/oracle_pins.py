@@ -178,6 +178,31 @@ def pin_decay_on_every_parameter(o, tmp):
         assert math.isclose(r["w"] - r["w_decayed"], -r["update"], rel_tol=1e-12)
 
 
+def pin_update_ranges_compose_to_the_step(o, tmp):
+    """Updating disjoint ranges that cover [0, n), each with the clip factor
+    of the whole gradient, is the full step bit for bit (the update of one
+    element depends on that element and s only)."""
+    rng = np.random.default_rng(23)
+    n = 1001
+    w0 = rng.normal(0, 0.05, n).astype(np.float32)
+    g = rng.normal(0, 0.3, n).astype(np.float32)
+    m0 = rng.normal(0, 0.01, n).astype(np.float32)
+    v0 = np.abs(rng.normal(0, 1e-3, n)).astype(np.float32)
+    wa, ma, va = w0.copy(), m0.copy(), v0.copy()
+    _, norm = o.adamw_clip_step(wa, g, ma, va, 5, 2e-3, 0.05, 1.0)
+    s = o.clip_scale(norm, 1.0)
+    assert s < 1.0
+    wb, mb, vb = w0.copy(), m0.copy(), v0.copy()
+    for lo, hi in ((700, 1001), (0, 1), (1, 333), (333, 333), (333, 700)):
+        o.adamw_update_range(wb, g, mb, vb, lo, hi, s, 5, 2e-3, 0.05)
+    assert wa.tobytes() == wb.tobytes() and ma.tobytes() == mb.tobytes()
+    assert va.tobytes() == vb.tobytes()
+    wc = w0.copy()
+    o.adamw_update_range(wc, g, m0.copy(), v0.copy(), 10, 20, s, 5, 2e-3, 0.05)
+    assert wc[:10].tobytes() == w0[:10].tobytes() and wc[20:].tobytes() == w0[20:].tobytes()
+    assert np.all(wc[10:20] != w0[10:20])
+
+
 # --- per-group weight decay ---------------------------------------------------
 
 _MASK_SIZES = (5, 3, 8, 1, 13, 4, 7, 2)

@@ -78,6 +78,9 @@ MUTANTS = {
                                 "double x = (double)g[i];\n        sumsq = sumsq + x * x;"),
     "scaled_update_unscaled": ("oracle_adamw_element((double)w[i], (double)g[i] * grad_scale,",
                                "oracle_adamw_element((double)w[i], (double)g[i],"),
+    "range_starts_late": ("for (int64_t j = lo; j < hi; ++j) {", "for (int64_t j = lo + 1; j < hi; ++j) {"),
+    "range_gradient_shifted": ("oracle_adamw_element((double)w[j], (double)g[j],",
+                               "oracle_adamw_element((double)w[j], (double)g[j + (j + 1 < hi)],"),
     "mask_ignored": ("double wd_k = decay[k] ? wd : 0.0;", "double wd_k = wd;"),
     "mask_inverted": ("double wd_k = decay[k] ? wd : 0.0;", "double wd_k = decay[k] ? 0.0 : wd;"),
     "mask_shifted": ("double wd_k = decay[k] ? wd : 0.0;",
