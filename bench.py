@@ -38,7 +38,11 @@ STEP_BYTES = 28      # fused kernel: read w, g, m, v; write w, m, v (float32)
 NORM_BYTES = 4       # norm kernel: read g
 PACK_BYTES = 24      # pack kernel: read w, m, v; write the staging image
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = {"k_clip_adamw": "step.cu", "k_grad_norm": "norm.cu", "k_ckpt_pack": "pack.cu"}
+# the source files each kernel is compiled from (its traffic record is tied
+# to their contents)
+KERNEL_SOURCES = {"k_clip_adamw": ("step.cu", "adamw_dev.cuh", "common.cuh", "internal.h"),
+                  "k_grad_norm": ("norm.cu", "norm_dev.cuh", "common.cuh", "internal.h"),
+                  "k_ckpt_pack": ("pack.cu", "common.cuh", "internal.h")}
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -81,13 +85,21 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_digest(kernel):
+    """sha256 prefix over the kernel's source files, in order."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "optimizer_step_resumable_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel, workload_name):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "optimizer_step_resumable_gb300", "csrc", KERNEL_SOURCES[kernel])
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = source_digest(kernel)
         for line in open(path):
             f = line.split()
             if len(f) >= 4 and f[0] == kernel and f[1] == workload_name and f[3] == digest:
@@ -638,7 +650,8 @@ def run_sweep(args):
     del w, m, v, g16, w_lp
     torch.cuda.empty_cache()
 
-    # latency case: 65,536 parameters (L2-resident), plain launches vs graph
+    # latency case: 65,536 parameters (L2-resident): host-driven steps and
+    # the GPU time of captured steps, one-launch vs two-launch
     wl = W.flat_65k()
     n = wl.n
     w = torch.empty(n, device=dev)
@@ -651,22 +664,44 @@ def run_sweep(args):
     with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
         osr.adamw_graph_create(ctx, w, g, m, v)
         out = {}
-        for mode in ("plain", "graph"):
+        # host-driven loops: the default step (one cooperative launch at this
+        # size), the two-launch step, the library's step graph
+        for mode in ("plain", "plain_two_launch", "graph"):
+            osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS
+                                         if mode == "plain_two_launch" else 0)
             for t in range(1, 50):
-                (osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip) if mode == "plain"
-                 else osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip))
+                (osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip) if mode == "graph"
+                 else osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip))
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             for t in range(50, 50 + steps):
-                if mode == "plain":
-                    osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
-                else:
+                if mode == "graph":
                     osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip)
+                else:
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
             b.record(main)
             b.synchronize()
             out[mode] = {"us_per_step": 1e3 * a.elapsed_time(b) / steps,
                          "params/s": n * steps / (a.elapsed_time(b) / 1e3)}
+        # GPU time per step: 50 steps captured into one graph and replayed
+        for mode in ("captured", "captured_two_launch"):
+            osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS
+                                         if mode == "captured_two_launch" else 0)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(gr, stream=cap):
+                    for _ in range(50):
+                        osr.adamw_clip_step(ctx, w, g, m, v, 100, wl.lr, wl.wd, wl.clip,
+                                            stream=cap)
+            gr.replay()
+            torch.cuda.synchronize()
+            ms, _, _ = median_ms(gr.replay, 20, main)
+            out[mode] = {"us_per_step": 1e3 * ms / 50, "params/s": n * 50 / (ms / 1e3)}
+            del gr
+        osr.adamw_set_launch_options(ctx, 0)
     row = {"workload": wl.name, "n": n, "latency": out}
     print(json.dumps(row), flush=True)
     return 0

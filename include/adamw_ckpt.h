@@ -72,7 +72,9 @@ extern "C" {
 #define ADAMW_DTYPE_F16 2  /* IEEE binary16                                */
 
 /* adamw_set_launch_options flags. */
-#define ADAMW_LAUNCH_NO_PDL 1 /* launch the fused kernel after the norm ends  */
+#define ADAMW_LAUNCH_NO_PDL 1     /* launch the fused kernel after the norm ends */
+#define ADAMW_LAUNCH_NO_ONEPASS 2 /* small states: two launches, not one         */
+#define ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT 4 /* tests only: see below          */
 
 /* adamw_clip_step_ex flags. */
 #define ADAMW_ZERO_GRAD 1    /* write 0 into g after reading it             */
@@ -296,6 +298,18 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * grid to complete before reading its result; results are unchanged.
  * ADAMW_LAUNCH_NO_PDL launches it in plain stream order instead.  (An
  * instrumentation event between the kernels also implies plain order.)
+ * States of up to 2^19 parameters (float32 gradient, 16-byte aligned arrays,
+ * no weight copy, no per-tensor norms, no global_sumsq) take the whole step
+ * as one cooperative launch instead (a cooperative kernel node when the
+ * stream is being captured): the same
+ * partial sums, the same fixed-order total and the same update, so the same
+ * bits, at half the launch cost.  Its blocks meet at a grid barrier whose
+ * wait is bounded (about one second); a wait that runs out skips the update
+ * and makes the next adamw_last_norm return ADAMW_ECUDA.
+ * ADAMW_LAUNCH_NO_ONEPASS always uses the two launches.
+ * ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT (for tests of that path): the next
+ * one-launch step waits for one block more than it launched, so its barrier
+ * runs out after about a second, as above.  Used once, then cleared.
  */
 ADAMW_API int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags);
 

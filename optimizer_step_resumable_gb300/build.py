@@ -24,8 +24,8 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler",
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
              "-I" + INCLUDE]
 
-CUDA_SOURCES = ["norm.cu", "step.cu", "pack.cu", "api.cu", "writer.cu", "graph.cu",
-                "noalloc.cu"]
+CUDA_SOURCES = ["norm.cu", "step.cu", "onepass.cu", "pack.cu", "api.cu", "writer.cu",
+                "graph.cu", "noalloc.cu"]
 CXX_SOURCES = ["ckpt_io.cpp", "manifest.cpp", "sha256.cpp"]
 
 
@@ -37,7 +37,8 @@ def nvcc() -> str:
 
 def _sources():
     return ([os.path.join(CSRC, s) for s in CUDA_SOURCES + CXX_SOURCES]
-            + [os.path.join(CSRC, h) for h in ("internal.h", "common.cuh", "context.h")]
+            + [os.path.join(CSRC, h) for h in ("internal.h", "common.cuh", "context.h",
+                                                 "norm_dev.cuh", "adamw_dev.cuh")]
             + [os.path.join(INCLUDE, "adamw_ckpt.h")])
 
 

@@ -54,6 +54,7 @@ private:
 };
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_state_ptr(const void* p, const char* name)
 {
@@ -177,7 +178,13 @@ int read_norm(adamw_ctx* c, double* norm_out, float* scale_out)
     if (!c->norm_launched)
         return fail(ADAMW_ESTATE, "no norm reduction has run on this context");
     CUDA_TRY(cudaEventSynchronize(c->ev_norm));
-    const volatile osr::NormResult* r = c->h_res;
+    volatile osr::NormResult* r = c->h_res;
+    if (r->fault) {
+        r->fault = 0u;
+        return fail(ADAMW_ECUDA,
+                    "the one-launch step's grid barrier wait ran out: that step skipped its "
+                    "update (w, m, v as before it)");
+    }
     const double norm = r->norm;
     const float scale = r->scale;
     const int nonfinite = r->nonfinite;
@@ -271,6 +278,13 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
         return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
     if (int qe = osr::query_pack_caps(c->sm_count, &c->caps))
         return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
+    {
+        int coop = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+        if (int qe = osr::query_onepass_blocks(c->sm_count, &c->onepass_capacity))
+            return bail(cuda_fail(cudaError_t(qe), "occupancy query"));
+        c->onepass_max_n = coop ? osr::kOnePassMaxN : 0;
+    }
 
     const size_t scratch = kScratchHead + sizeof(double) * osr::kNormBlocksMax;
     if ((e = cudaMalloc(&c->d_scratch, scratch)) != cudaSuccess)
@@ -279,6 +293,9 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
         return bail(cuda_fail(e, "cudaMemset(norm scratch)"));
     c->d_res = reinterpret_cast<osr::NormResult*>(c->d_scratch);
     c->d_counter = reinterpret_cast<unsigned int*>(c->d_scratch + sizeof(osr::NormResult));
+    c->d_bar = reinterpret_cast<uint32_t*>(c->d_scratch + 64);
+    static_assert(sizeof(osr::NormResult) + sizeof(unsigned int) <= 64 && 64 + 8 <= kScratchHead,
+                  "scratch head layout");
     c->d_partials = reinterpret_cast<double*>(c->d_scratch + kScratchHead);
     if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_res), sizeof(osr::NormResult),
                            cudaHostAllocMapped)) != cudaSuccess) {
@@ -511,6 +528,26 @@ int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype
     ctx->prof[0] = ctx->prof[1] = ctx->prof[2] = nullptr;
     if (prof[0])
         CUDA_TRY(cudaEventRecord(prof[0], st));
+    // Small states: the whole step as one cooperative launch (same bits as
+    // the two launches below), also when captured into a graph (a
+    // cooperative kernel node); not when an event was asked for between the
+    // two kernels.
+    if (!external && g_dtype == ADAMW_DTYPE_F32 && !d_w_lp && !(flags & ADAMW_TENSOR_NORMS) &&
+        !prof[1] && ctx->onepass && ctx->n <= ctx->onepass_max_n &&
+        osr::onepass_grid(ctx->n, ctx->onepass_capacity) <= ctx->onepass_capacity &&
+        aligned16(d_w) && aligned16(d_g) && aligned16(d_m) && aligned16(d_v)) {
+        const bool fault_test = ctx->onepass_fault_test;
+        ctx->onepass_fault_test = false;
+        const int e = osr::launch_onepass(
+            d_w, static_cast<float*>(d_g), d_m, d_v, ctx->n, k, clip, grad_scale,
+            ctx->d_partials, ctx->d_bar, fault_test, ctx->d_res, ctx->h_res_dev,
+            ctx->onepass_capacity, (flags & ADAMW_ZERO_GRAD) != 0, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(cudaError_t(e), "one-launch step");
+        if (prof[2])
+            CUDA_TRY(cudaEventRecord(prof[2], st));
+        return mark_norm(ctx, st);
+    }
     if (!external) {
         rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale,
                             (flags & ADAMW_TENSOR_NORMS) != 0, g_dtype);
@@ -568,9 +605,11 @@ int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags)
     osr::clear_error();
     if (!ctx)
         return fail(ADAMW_EINVAL, "ctx is NULL");
-    if (flags & ~ADAMW_LAUNCH_NO_PDL)
+    if (flags & ~(ADAMW_LAUNCH_NO_PDL | ADAMW_LAUNCH_NO_ONEPASS | ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT))
         return fail(ADAMW_EINVAL, "unknown launch flags 0x%x", flags);
     ctx->pdl = !(flags & ADAMW_LAUNCH_NO_PDL);
+    ctx->onepass = !(flags & ADAMW_LAUNCH_NO_ONEPASS);
+    ctx->onepass_fault_test = (flags & ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT) != 0;
     return ADAMW_OK;
 }
 

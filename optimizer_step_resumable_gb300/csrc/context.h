@@ -41,7 +41,7 @@ struct adamw_ctx {
     osr::KernelCaps caps{};
     double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
 
-    // norm scratch: [NormResult | counter | pad][partials x kNormBlocksMax]
+    // norm scratch: [NormResult | counter | barrier x 2 | pad][partials x kNormBlocksMax]
     unsigned char* d_scratch = nullptr;
     osr::NormResult* d_res = nullptr;
     unsigned int* d_counter = nullptr;
@@ -63,6 +63,14 @@ struct adamw_ctx {
     bool segs_launched = false;        // the last reduction also wrote segments
     cudaEvent_t prof[3] = {nullptr, nullptr, nullptr};  // one-shot instrumentation
     bool pdl = true;  // launch the fused kernel as a programmatic dependent
+    // One-launch step for small states: cooperative grid capacity, barrier
+    // counters (in the scratch head), enabled, size limit, one-shot test of
+    // the barrier timeout.
+    int onepass_capacity = 0;
+    uint32_t* d_bar = nullptr;
+    bool onepass = true;
+    int64_t onepass_max_n = 0;
+    bool onepass_fault_test = false;
     // Per-tensor decay flags expanded to one bit per element (allocated by
     // the first adamw_set_decay_mask that exempts a tensor).
     uint32_t* d_decay_mask = nullptr;

@@ -29,7 +29,8 @@ struct NormResult {
     float scale;        // factor applied to raw g: grad_scale * clip factor
     int32_t nonfinite;  // 1 if norm is inf or nan (the step is skipped)
     uint32_t seq;       // incremented by every reduction (host staleness check)
-    uint32_t pad;
+    uint32_t fault;     // host mirror only: set by a one-launch step whose grid
+                        // barrier wait ran out; cleared by the host
 };
 
 // Per-step scalars, computed on the host in double and rounded to float once.
@@ -110,6 +111,20 @@ int launch_adamw(float* w, const void* g, float* m, float* v, int64_t n,
                  const KernelCaps& caps, void* stream, bool zero_grad = false,
                  bool programmatic = false, int32_t g_dtype = kDtypeF32,
                  void* w_lp = nullptr, int32_t w_lp_dtype = kDtypeBF16);
+// The one-launch step (onepass.cu): norm, clip factor and update in one
+// cooperative grid of onepass_grid(n, capacity) blocks; bar: two zeroed
+// uint32 barrier counters; fault_test: wait for one block more than the grid
+// has (the barrier times out).  w, g, m, v 16-byte aligned, float32 g.
+int query_onepass_blocks(int sm_count, int* blocks_out);
+int onepass_grid(int64_t n, int capacity);
+int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const StepScalars& k,
+                   double clip, double grad_scale, double* partials, uint32_t* bar,
+                   bool fault_test, NormResult* d_res, NormResult* h_res, int capacity,
+                   bool zero_grad, void* stream);
+// States up to this many parameters take the one-launch step by default
+// (measured on GB300: below about 2^20 it saves 2 us per step; from 2^20 up
+// the two launches, which overlap, are faster).
+constexpr int64_t kOnePassMaxN = int64_t(1) << 19;
 int launch_pack(const float* w, const float* m, const float* v, int64_t n,
                 int32_t step, unsigned char* image, const KernelCaps& caps,
                 void* stream);

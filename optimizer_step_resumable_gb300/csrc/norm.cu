@@ -15,79 +15,15 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "norm_dev.cuh"
 
 namespace osr {
 namespace {
 
 using detail::block_sum;
 
-// (a^2 + b^2) + (c^2 + d^2): two fused multiply-adds and one add, each
-// correctly rounded in float32.
-__device__ __forceinline__ float sumsq4(float4 a)
-{
-    return __fadd_rn(__fmaf_rn(a.x, a.x, __fmul_rn(a.y, a.y)),
-                     __fmaf_rn(a.z, a.z, __fmul_rn(a.w, a.w)));
-}
-
-// Sum of squares of one run of 4*U values.  Fast path: float32 squares,
-// pairwise tree (depth 2 + log2 U), so the relative error is at most about
-// (3 + log2 U) units of 2^-24 -- 3.6e-7 for U = 8 -- and the run is flushed
-// into the caller's double accumulator.  Runs whose float32 sum leaves
-// [2^-100, FLT_MAX] (overflow, inf, nan, or values so small that squares
-// underflow) are recomputed exactly in double; all-zero runs (common for
-// embedding rows no token touched) skip that and contribute 0.
-template <int U>
-__device__ __forceinline__ double run_sumsq(const float4 (&x)[U])
-{
-    float q[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-        q[j] = sumsq4(x[j]);
-#pragma unroll
-    for (int s = 1; s < U; s <<= 1)
-#pragma unroll
-        for (int j = 0; j + s < U; j += 2 * s)
-            q[j] = __fadd_rn(q[j], q[j + s]);
-    const float r = q[0];
-    if (r >= 0x1p-100f && r <= FLT_MAX)
-        return double(r);
-    unsigned bits = 0;
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-        bits |= (__float_as_uint(x[j].x) | __float_as_uint(x[j].y) |
-                 __float_as_uint(x[j].z) | __float_as_uint(x[j].w)) & 0x7fffffffu;
-    if (bits == 0)
-        return 0.0;
-    double d = 0.0;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-        d += double(x[j].x) * double(x[j].x);
-        d += double(x[j].y) * double(x[j].y);
-        d += double(x[j].z) * double(x[j].z);
-        d += double(x[j].w) * double(x[j].w);
-    }
-    return d;
-}
-
-// This thread's share of one tile restricted to elements [lo, hi): exact
-// double squares (used only on tiles where a tensor of the offset table
-// starts, to split the tile between tensors).
-template <int U>
-__device__ __forceinline__ double thread_sumsq_in(const float4 (&x)[U], int64_t base, int tid,
-                                                  int64_t lo, int64_t hi)
-{
-    double d = 0.0;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-        const int64_t e = base + (int64_t(j * kNormThreads + tid) << 2);
-        const float c[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (e + q >= lo && e + q < hi)
-                d += double(c[q]) * double(c[q]);
-    }
-    return d;
-}
+using normdev::run_sumsq;
+using normdev::thread_sumsq_in;
 
 // ---------------------------------------------------------------------------
 // Global L2 norm, two levels in one launch.
@@ -142,28 +78,7 @@ __global__ void __launch_bounds__(kNormThreads, 4)
     for (int64_t tile = t_lo; tile < t_hi; ++tile) {
         const int64_t base = tile * kNormTileElems;
         float4 x[U];
-        if (tile < nfull) {
-            if constexpr (kVec) {
-#pragma unroll
-                for (int j = 0; j < U; ++j)
-                    x[j] = detail::load4_cs<G>(g + base + (int64_t(j * kNormThreads + tid) << 2));
-            } else {  // float32 at a 4-byte (not 16-byte) boundary
-#pragma unroll
-                for (int j = 0; j < U; ++j) {
-                    const G* p = g + base + (int64_t(j * kNormThreads + tid) << 2);
-                    x[j] = make_float4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const int64_t e = base + (int64_t(j * kNormThreads + tid) << 2);
-                x[j].x = e < n ? detail::load1(g + e) : 0.0f;
-                x[j].y = e + 1 < n ? detail::load1(g + e + 1) : 0.0f;
-                x[j].z = e + 2 < n ? detail::load1(g + e + 2) : 0.0f;
-                x[j].w = e + 3 < n ? detail::load1(g + e + 3) : 0.0f;
-            }
-        }
+        normdev::load_tile<U, kVec, G>(g, n, nfull, tile, tid, x);
         const double r = run_sumsq<U>(x);
         acc += r;
         if (kSegs) {
@@ -208,31 +123,10 @@ __global__ void __launch_bounds__(kNormThreads, 4)
     if (!is_last)
         return;
     __threadfence();
-    double s = 0.0;
-    for (int i = tid; i < int(gridDim.x); i += kNormThreads)
-        s += __ldcg(partials + i);
-    s = block_sum<kNormThreads>(s);
+    const double s = normdev::sum_partials(partials, int(gridDim.x));
     if (tid == 0) {
-        NormResult r;
-        r.sumsq = s;
-        // the norm of the scaled gradient grad_scale * g, and the factor
-        // applied to raw g (grad_scale times the clip factor), rounded once
-        r.norm = grad_scale * sqrt(s);
-        const bool finite = isfinite(r.norm);
-        r.nonfinite = finite ? 0 : 1;
-        r.scale = float(grad_scale * ((finite && r.norm > clip) ? clip / r.norm : 1.0));
-        r.seq = d_res->seq + 1u;
-        r.pad = 0;
-        *d_res = r;
-        if (h_res) {
-            volatile NormResult* h = h_res;
-            h->sumsq = r.sumsq;
-            h->norm = r.norm;
-            h->scale = r.scale;
-            h->nonfinite = r.nonfinite;
-            h->seq = r.seq;
-            __threadfence_system();
-        }
+        normdev::publish(normdev::make_result(s, clip, grad_scale, d_res->seq + 1u), d_res,
+                         h_res);
         *counter = 0u;
     }
 }
