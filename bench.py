@@ -65,6 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="per-size kernel measurements (flat 2^20..2^30, latency at 65,536); "
                         "prints one JSON object per size instead of the bench line")
+    p.add_argument("--sweep-latency-only", action="store_true",
+                   help="with --sweep: only the latency case at 65,536")
     return p.parse_args(argv)
 
 
@@ -543,7 +545,7 @@ def run_sweep(args):
     peak, peak_kind = measured_peaks()
     flush = torch.ones(128 << 20, device=dev)
     rows = []
-    for log2n in range(20, 31):
+    for log2n in range(20, 31) if not args.sweep_latency_only else ():
         wl = W.flat_pow2(log2n)
         n = wl.n
         w = torch.empty(n, device=dev)
@@ -617,8 +619,20 @@ def run_sweep(args):
         del w, g, m, v
         torch.cuda.empty_cache()
 
-    # mixed precision on the 110M tensor list: bfloat16 gradient, bfloat16
-    # copy of the new weights (2 + 28 bytes per parameter)
+    if not args.sweep_latency_only:
+        sweep_mixed(dev, main, flush, peak)
+    sweep_latency(dev, main)
+    return 0
+
+
+def sweep_mixed(dev, main, flush, peak):
+    """Mixed precision on the 110M tensor list: bfloat16 gradient, bfloat16
+    copy of the new weights (2 + 28 bytes per parameter)."""
+    import torch
+
+    import optimizer_step_resumable_gb300 as osr
+    from synthetic import device as synth_dev
+    from synthetic import workloads as W
     wl = W.gpt_110m()
     n = wl.n
     off, num = wl.table()
@@ -650,8 +664,15 @@ def run_sweep(args):
     del w, m, v, g16, w_lp
     torch.cuda.empty_cache()
 
-    # latency case: 65,536 parameters (L2-resident): host-driven steps and
-    # the GPU time of captured steps, one-launch vs two-launch
+
+def sweep_latency(dev, main):
+    """Latency case: 65,536 parameters (L2-resident): host-driven steps and
+    the GPU time of captured steps, one-launch vs two-launch."""
+    import torch
+
+    import optimizer_step_resumable_gb300 as osr
+    from synthetic import device as synth_dev
+    from synthetic import workloads as W
     wl = W.flat_65k()
     n = wl.n
     w = torch.empty(n, device=dev)
@@ -665,18 +686,21 @@ def run_sweep(args):
         osr.adamw_graph_create(ctx, w, g, m, v)
         out = {}
         # host-driven loops: the default step (one cooperative launch at this
-        # size), the two-launch step, the library's step graph
-        for mode in ("plain", "plain_two_launch", "graph"):
+        # size), the two-launch step, the library's step graph (one
+        # cooperative node at this size, or the two-node graph)
+        for mode in ("plain", "plain_two_launch", "graph", "graph_two_node"):
             osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS
-                                         if mode == "plain_two_launch" else 0)
+                                         if mode.endswith("two_launch") or
+                                         mode.endswith("two_node") else 0)
+            graph = mode.startswith("graph")
             for t in range(1, 50):
-                (osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip) if mode == "graph"
+                (osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip) if graph
                  else osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip))
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             for t in range(50, 50 + steps):
-                if mode == "graph":
+                if graph:
                     osr.adamw_graph_step(ctx, t, wl.lr, wl.wd, wl.clip)
                 else:
                     osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)

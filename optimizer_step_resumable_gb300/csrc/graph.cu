@@ -1,5 +1,6 @@
 // graph.cu -- one optimizer step as a CUDA graph (norm kernel node, then the
-// fused clip+AdamW node) for states small enough that launch latency
+// fused clip+AdamW node; for states the one-launch step serves, that step as
+// one cooperative node) for states small enough that launch latency
 // dominates.  The per-step scalars (bias corrections depend on t) are kernel
 // arguments, so each step rewrites the two nodes' parameters in the
 // instantiated graph (cudaGraphExecKernelNodeSetParams, which leaves launches
@@ -56,12 +57,70 @@ int cuda_fail(cudaError_t e, const char* what)
     return fail(ADAMW_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether the graph takes the one-launch step (the same rule as
+// adamw_clip_step's).
+bool want_onepass(const adamw_ctx* c)
+{
+    return c->onepass && c->n <= c->onepass_max_n &&
+           onepass_grid(c->n, c->onepass_capacity) <= c->onepass_capacity &&
+           aligned16(c->graph_w) && aligned16(c->graph_g) && aligned16(c->graph_m) &&
+           aligned16(c->graph_v);
+}
+
+void fill_onepass(const adamw_ctx* c, double clip, const StepScalars& k, bool fault_test,
+                  OnepassNodeArgs* a, cudaKernelNodeParams* p)
+{
+    a->w = c->graph_w;
+    a->g = const_cast<float*>(c->graph_g);
+    a->m = c->graph_m;
+    a->v = c->graph_v;
+    a->n = c->n;
+    a->k = k;
+    a->clip = clip;
+    a->grad_scale = 1.0;
+    a->partials = c->d_partials;
+    a->bar = c->d_bar;
+    a->d_res = c->d_res;
+    a->h_res = c->h_res_dev;
+    onepass_node_params(a, c->onepass_capacity, fault_test, p);
+}
+
 // Builds and instantiates the two-node graph over the context's graph_*
 // pointers.  The fused node's kernel variant depends on whether decay flags
 // are set (an instantiated node cannot change its function), so the graph
 // remembers that and is rebuilt when it changes.
 int graph_build(adamw_ctx* ctx)
 {
+    if (want_onepass(ctx)) {
+        OnepassNodeArgs oa;
+        cudaKernelNodeParams op{};
+        fill_onepass(ctx, INFINITY, make_step_scalars(ctx, 1, 0.0, 0.0), false, &oa, &op);
+        cudaLaunchAttributeValue coop{};
+        coop.cooperative = 1;
+        cudaError_t e;
+        int rc = ADAMW_OK;
+        if ((e = cudaGraphCreate(&ctx->graph, 0)) != cudaSuccess)
+            rc = cuda_fail(e, "cudaGraphCreate");
+        else if ((e = cudaGraphAddKernelNode(&ctx->graph_norm, ctx->graph, nullptr, 0, &op)) !=
+                 cudaSuccess)
+            rc = cuda_fail(e, "cudaGraphAddKernelNode(one-launch step)");
+        else if ((e = cudaGraphKernelNodeSetAttribute(ctx->graph_norm,
+                                                      cudaLaunchAttributeCooperative, &coop)) !=
+                 cudaSuccess)
+            rc = cuda_fail(e, "cudaGraphKernelNodeSetAttribute(cooperative)");
+        else if ((e = cudaGraphInstantiate(&ctx->graph_exec, ctx->graph, 0)) != cudaSuccess)
+            rc = cuda_fail(e, "cudaGraphInstantiate");
+        if (rc != ADAMW_OK) {
+            graph_release(ctx);
+        } else {
+            ctx->graph_mask = ctx->decay_mask_on;
+            ctx->graph_onepass = true;
+        }
+        return rc;
+    }
+    ctx->graph_onepass = false;
     NormNodeArgs na;
     AdamwNodeArgs aa;
     cudaKernelNodeParams np{}, ap{};
@@ -132,8 +191,9 @@ int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd, double cli
     if (prev != ctx->device)
         cudaSetDevice(ctx->device);
     int rc = ADAMW_OK;
-    if (ctx->graph_mask != ctx->decay_mask_on) {
-        // decay flags set or cleared since the graph was built
+    if (ctx->graph_mask != ctx->decay_mask_on || ctx->graph_onepass != osr::want_onepass(ctx)) {
+        // decay flags set or cleared, or the one-launch option changed, since
+        // the graph was built
         float* w = ctx->graph_w;
         const float* g = ctx->graph_g;
         float* m = ctx->graph_m;
@@ -152,19 +212,30 @@ int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd, double cli
     }
     osr::NormNodeArgs na;
     osr::AdamwNodeArgs aa;
+    osr::OnepassNodeArgs oa;
     cudaKernelNodeParams np{}, ap{};
-    osr::fill_args(ctx, clip, osr::make_step_scalars(ctx, t, lr, wd), &na, &aa, &np, &ap);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_norm, &np)) !=
-        cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(norm)");
-    else if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_step, &ap)) !=
-             cudaSuccess)
-        rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(step)");
-    else if ((e = cudaGraphLaunch(ctx->graph_exec, s)) != cudaSuccess)
+    if (ctx->graph_onepass) {
+        const bool fault_test = ctx->onepass_fault_test;
+        ctx->onepass_fault_test = false;
+        osr::fill_onepass(ctx, clip, osr::make_step_scalars(ctx, t, lr, wd), fault_test, &oa,
+                          &np);
+        if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_norm, &np)) !=
+            cudaSuccess)
+            rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(one-launch step)");
+    } else {
+        osr::fill_args(ctx, clip, osr::make_step_scalars(ctx, t, lr, wd), &na, &aa, &np, &ap);
+        if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_norm, &np)) !=
+            cudaSuccess)
+            rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(norm)");
+        else if ((e = cudaGraphExecKernelNodeSetParams(ctx->graph_exec, ctx->graph_step, &ap)) !=
+                 cudaSuccess)
+            rc = osr::cuda_fail(e, "cudaGraphExecKernelNodeSetParams(step)");
+    }
+    if (rc == ADAMW_OK && (e = cudaGraphLaunch(ctx->graph_exec, s)) != cudaSuccess)
         rc = osr::cuda_fail(e, "cudaGraphLaunch");
-    else {
+    if (rc == ADAMW_OK) {
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         cudaStreamIsCapturing(s, &cap);
         if (cap == cudaStreamCaptureStatusNone) {

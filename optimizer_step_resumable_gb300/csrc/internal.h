@@ -153,11 +153,31 @@ struct AdamwNodeArgs {
     void* w_lp;  // always NULL in the step graph
     void* ptrs[8];
 };
+// The one-launch step as a single (cooperative) graph node.
+struct OnepassNodeArgs {
+    float* w;
+    float* g;
+    float* m;
+    float* v;
+    int64_t n;
+    StepScalars k;
+    double clip, grad_scale;
+    double* partials;
+    int32_t P;
+    uint32_t* bar;
+    uint32_t expect;
+    NormResult* d_res;
+    NormResult* h_res;
+    void* ptrs[14];
+};
 }  // namespace osr
 struct cudaKernelNodeParams;
 namespace osr {
 int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p);
 int adamw_node_params(AdamwNodeArgs* a, const KernelCaps& caps, cudaKernelNodeParams* p);
+// fault_test: the node's barrier waits for one block more than its grid.
+int onepass_node_params(OnepassNodeArgs* a, int capacity, bool fault_test,
+                        cudaKernelNodeParams* p);
 
 // Host file I/O (ckpt_io.cpp).
 constexpr size_t kIoBlock = 4096;  // O_DIRECT alignment of address, length and offset

@@ -186,6 +186,37 @@ int onepass_grid(int64_t n, int capacity)
     return blocks > P ? blocks : P;
 }
 
+int onepass_node_params(OnepassNodeArgs* a, int capacity, bool fault_test,
+                        cudaKernelNodeParams* p)
+{
+    const int blocks = onepass_grid(a->n, capacity);
+    a->P = norm_blocks(a->n);
+    a->expect = uint32_t(blocks) + (fault_test ? 1u : 0u);
+    void** q = a->ptrs;
+    q[0] = &a->w;
+    q[1] = &a->g;
+    q[2] = &a->m;
+    q[3] = &a->v;
+    q[4] = &a->n;
+    q[5] = &a->k;
+    q[6] = &a->clip;
+    q[7] = &a->grad_scale;
+    q[8] = &a->partials;
+    q[9] = &a->P;
+    q[10] = &a->bar;
+    q[11] = &a->expect;
+    q[12] = &a->d_res;
+    q[13] = &a->h_res;
+    p->func = a->k.decay_mask ? reinterpret_cast<void*>(&k_clip_adamw_onepass<false, true>)
+                              : reinterpret_cast<void*>(&k_clip_adamw_onepass<false, false>);
+    p->gridDim = dim3(unsigned(blocks));
+    p->blockDim = dim3(kNormThreads);
+    p->sharedMemBytes = 0;
+    p->kernelParams = a->ptrs;
+    p->extra = nullptr;
+    return blocks <= capacity ? 0 : int(cudaErrorCooperativeLaunchTooLarge);
+}
+
 int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const StepScalars& k,
                    double clip, double grad_scale, double* partials, uint32_t* bar,
                    bool fault_test, NormResult* d_res, NormResult* h_res, int capacity,

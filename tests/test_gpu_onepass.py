@@ -143,3 +143,64 @@ def test_captured_one_launch_steps_match_eager_two_launch_steps(dev):
     del gr
     ctx_a.close()
     ctx_b.close()
+
+
+def test_step_graph_one_node_matches_plain_steps(dev):
+    """The library's step graph at a one-launch size is one cooperative node;
+    through a sequence that sets decay flags, switches the one-launch step
+    off and on again (each change rebuilds the graph), its steps equal plain
+    two-launch steps bit for bit."""
+    sizes = [1000, 3, 60_000, 5, 4_536]
+    num = np.array(sizes, np.int64)
+    off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
+    n = int(num.sum())
+    hw, hm, hv = inputs(n)
+    hg = synthetic.grads(7, 1, 1e-2, n=n, outlier_frac=0.01, outlier_mult=100.0)
+    plan = {2: ("mask", [1, 0, 1, 1, 0]), 4: ("opts", osr.LAUNCH_NO_ONEPASS), 5: ("opts", 0),
+            6: ("mask", None)}
+    outs, norms = [], []
+    for use_graph in (False, True):
+        w, g, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv))
+        got_norms = []
+        with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+            if not use_graph:
+                osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS)
+            else:
+                osr.adamw_graph_create(ctx, w, g, m, v)
+            for t in range(1, 8):
+                kind, val = plan.get(t, (None, None))
+                if kind == "mask":
+                    osr.adamw_set_decay_mask(ctx, val)
+                elif kind == "opts" and use_graph:
+                    osr.adamw_set_launch_options(ctx, val)
+                if use_graph:
+                    osr.adamw_graph_step(ctx, t, LR, WD, CLIP)
+                else:
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, LR, WD, CLIP)
+                got_norms.append(osr.adamw_last_norm(ctx))
+            if use_graph:
+                osr.adamw_graph_destroy(ctx)
+        outs.append([x.cpu().numpy().tobytes() for x in (w, m, v)])
+        norms.append(got_norms)
+    assert outs[0] == outs[1]
+    assert norms[0] == norms[1]
+
+
+def test_step_graph_barrier_timeout_is_reported(dev):
+    n = 40_000
+    hw, hm, hv = inputs(n)
+    w, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hm, hv))
+    g = torch.from_numpy(synthetic.grads(7, 1, 1e-2, n=n)).to(dev)
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_graph_create(ctx, w, g, m, v)
+        osr.adamw_set_launch_options(ctx, osr.LAUNCH_TEST_BARRIER_TIMEOUT)
+        osr.adamw_graph_step(ctx, 1, LR, WD, CLIP)
+        with pytest.raises(osr.AdamWError) as e:
+            osr.adamw_last_norm(ctx)
+        assert e.value.status == osr.ECUDA
+        for d, h in zip((w, m, v), (hw, hm, hv)):
+            assert d.cpu().numpy().tobytes() == h.tobytes()
+        osr.adamw_graph_step(ctx, 1, LR, WD, CLIP)
+        osr.adamw_last_norm(ctx)
+        assert not torch.equal(w, torch.from_numpy(hw).to(dev))
+        osr.adamw_graph_destroy(ctx)
