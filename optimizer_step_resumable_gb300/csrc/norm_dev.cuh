@@ -151,7 +151,10 @@ __device__ __forceinline__ NormResult make_result(double s, double clip, double 
 
 // Writes r to the device record and, if given, its host-mapped mirror, field
 // by field; the fault word is left alone (only a timed-out wait sets it and
-// only the host clears it).
+// only the host clears it).  No system-scope fence: the host reads the
+// mirror only after synchronizing with an event recorded behind this grid,
+// and a grid's writes to mapped memory are visible once it has completed (a
+// fence here cost about 2 us at the end of every reduction).
 __device__ __forceinline__ void publish(const NormResult& r, NormResult* d_res,
                                         NormResult* h_res)
 {
@@ -167,7 +170,6 @@ __device__ __forceinline__ void publish(const NormResult& r, NormResult* d_res,
         h->scale = r.scale;
         h->nonfinite = r.nonfinite;
         h->seq = r.seq;
-        __threadfence_system();
     }
 }
 
