@@ -223,13 +223,16 @@ ADAMW_API int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void
  * One step as a CUDA graph, for states small enough that launch latency
  * dominates (e.g. 65,536 parameters: L2-resident, a few microseconds per
  * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm
- * kernel followed by the fused clip+AdamW kernel (same kernels, same results
- * bit for bit as adamw_clip_step) and instantiates it; the context owns it
- * (replaced by the next adamw_graph_create, freed by adamw_graph_destroy or
- * adamw_destroy).  adamw_graph_step writes step t's scalars (t, lr, wd, clip;
- * bias corrections in double on the host) into the graph's two kernel nodes
- * and launches it on `stream` -- one launch per step.  adamw_last_norm
- * reports its norm.  ADAMW_ESTATE if no graph was created.
+ * kernel followed by the fused clip+AdamW kernel -- or, where adamw_clip_step
+ * would take the one-launch step (see adamw_set_launch_options), that step
+ * as one cooperative kernel node -- with the same results bit for bit as
+ * adamw_clip_step, and instantiates it; the context owns it (replaced by the
+ * next adamw_graph_create, freed by adamw_graph_destroy or adamw_destroy).
+ * adamw_graph_step writes step t's scalars (t, lr, wd, clip; bias
+ * corrections in double on the host) into the graph's kernel nodes and
+ * launches it on `stream` -- one launch per step; it first rebuilds the
+ * graph if decay flags or the one-launch option changed since it was made.
+ * adamw_last_norm reports its norm.  ADAMW_ESTATE if no graph was created.
  */
 ADAMW_API int adamw_graph_create(adamw_ctx* ctx, float* d_w, const float* d_g,
                                  float* d_m, float* d_v);
