@@ -586,6 +586,22 @@ def run_sweep(args):
 
         pack_ms, _, _ = median_ms(pack, max(3, reps // 2), main)
         osr.ckpt_wait(ctx)
+        # the pack kernel alone: the copy goes to another stream, so the
+        # events on the main stream bracket the kernel only
+        side = torch.cuda.Stream()
+
+        def pack_only():
+            osr.ckpt_pack(ctx, 1, w, m, v, main_stream=main, side_stream=side)
+
+        pack_only()
+        torch.cuda.synchronize()
+        pack_k = []
+        for _ in range(max(3, reps // 2)):
+            flush.sum()
+            torch.cuda.synchronize()
+            pack_k.append(median_ms(pack_only, 1, main)[0])
+            torch.cuda.synchronize()
+        pack_kernel_ms = statistics.median(pack_k)
         # GPU time per step without launch overhead: 50 steps in one graph
         # (t fixed inside the graph; the kernels' work does not depend on t)
         torch.cuda.synchronize()
@@ -613,6 +629,8 @@ def run_sweep(args):
                "step_graph": {"ms": graph_step_ms, "params/s": n / (graph_step_ms / 1e3),
                               "GB/s": 32 * n / graph_step_ms / 1e6},
                "pack+d2h": {"ms": pack_ms, "GB/s(device 24n)": 24 * n / pack_ms / 1e6},
+               "k_ckpt_pack": {"ms": pack_kernel_ms, "GB/s": 24 * n / pack_kernel_ms / 1e6,
+                               "frac": 24 * n / pack_kernel_ms / 1e6 / peak},
                "peak_GB/s": peak, "peak_kind": peak_kind}
         rows.append(row)
         print(json.dumps(row), flush=True)

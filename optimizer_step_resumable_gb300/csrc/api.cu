@@ -350,7 +350,7 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
     }
 
     if (!(flags & ADAMW_CREATE_NO_CKPT)) {
-        const size_t bytes = 16 + size_t(12) * size_t(n_params);
+        const size_t bytes = c->stage_bytes();
         if ((e = cudaMalloc(&c->d_image_alloc, bytes)) != cudaSuccess) {
             c->d_image_alloc = nullptr;
             return bail(cuda_fail(e, "cudaMalloc(checkpoint staging)"));
@@ -686,15 +686,22 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
     // The staging image may still be read by the previous copy.
     if (ctx->d2h_pending)
         CUDA_TRY(cudaStreamWaitEvent(mainst, ctx->ev_d2h, 0));
-    const int e = osr::launch_pack(d_w, d_m, d_v, ctx->n, step, ctx->d_image(), ctx->caps,
+    const int e = osr::launch_pack(d_w, d_m, d_v, ctx->n, step, ctx->d_stage(0),
+                                   reinterpret_cast<float*>(ctx->d_stage(1)),
+                                   reinterpret_cast<float*>(ctx->d_stage(2)),
+                                   reinterpret_cast<float*>(ctx->d_stage(3)), ctx->caps,
                                    main_stream);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "pack kernel launch");
     CUDA_TRY(cudaEventRecord(ctx->ev_pack, mainst));
     if (side != mainst)
         CUDA_TRY(cudaStreamWaitEvent(side, ctx->ev_pack, 0));
-    CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_image(), ctx->image_bytes(),
-                             cudaMemcpyDeviceToHost, side));
+    // the header and the three regions to their file offsets in the image
+    const size_t rb = size_t(4) * size_t(ctx->n);
+    CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_stage(0), 8, cudaMemcpyDeviceToHost, side));
+    for (int r = 1; r <= 3; ++r)
+        CUDA_TRY(cudaMemcpyAsync(ctx->h_image() + 8 + size_t(r - 1) * rb, ctx->d_stage(r), rb,
+                                 cudaMemcpyDeviceToHost, side));
     CUDA_TRY(cudaEventRecord(ctx->ev_d2h, side));
     ctx->packed = true;
     ctx->d2h_pending = true;

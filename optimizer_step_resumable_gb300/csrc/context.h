@@ -76,11 +76,13 @@ struct adamw_ctx {
     uint32_t* d_decay_mask = nullptr;
     bool decay_mask_on = false;
 
-    // Checkpoint staging.  Device image at alloc + 8, so that its w region
-    // (image + 8) starts on a 16-byte boundary for the pack kernel's vector
-    // stores; pinned host image at the (page-aligned) start of its
-    // allocation, padded to a whole number of 4 KiB blocks, so that the
-    // writer can hand it to the disk with O_DIRECT.
+    // Checkpoint staging.  On the device: the 8-byte header and the w, m, v
+    // regions each in its own 256-byte aligned slot (d_stage(r), r = 0 for the
+    // header, 1..3 for w, m, v), so that the pack kernel's stores start on
+    // cache-line boundaries; the copy to the host puts them at their file
+    // offsets.  On the host: the file image, contiguous, at the (page-aligned)
+    // start of its allocation, padded to a whole number of 4 KiB blocks, so
+    // that the writer can hand it to the disk with O_DIRECT.
     bool has_ckpt = false;
     unsigned char* d_image_alloc = nullptr;
     unsigned char* h_image_alloc = nullptr;
@@ -104,7 +106,16 @@ struct adamw_ctx {
     int32_t write_flags = osr::kWriteDirect;
     osr::WriterState writer;
 
-    unsigned char* d_image() const { return d_image_alloc + 8; }
+    static constexpr size_t kStageAlign = 256;
+    size_t stage_region_bytes() const
+    {
+        return (size_t(4) * size_t(n) + kStageAlign - 1) / kStageAlign * kStageAlign;
+    }
+    size_t stage_bytes() const { return kStageAlign + 3 * stage_region_bytes(); }
+    unsigned char* d_stage(int r) const
+    {
+        return d_image_alloc + (r == 0 ? 0 : kStageAlign + size_t(r - 1) * stage_region_bytes());
+    }
     unsigned char* h_image() const { return h_image_alloc; }
     size_t image_bytes() const { return size_t(8 + 12 * n); }
     size_t h_image_capacity() const { return osr::round_up_block(image_bytes()); }

@@ -125,8 +125,10 @@ int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const Step
 // (measured on GB300: below about 2^20 it saves 2 us per step; from 2^20 up
 // the two launches, which overlap, are faster).
 constexpr int64_t kOnePassMaxN = int64_t(1) << 19;
-int launch_pack(const float* w, const float* m, const float* v, int64_t n,
-                int32_t step, unsigned char* image, const KernelCaps& caps,
+// The pack: header (8 bytes, 8-byte aligned) and the w, m, v regions
+// (16-byte aligned; 256-byte aligned for full speed) of the staging buffer.
+int launch_pack(const float* w, const float* m, const float* v, int64_t n, int32_t step,
+                unsigned char* header, float* dw, float* dm, float* dv, const KernelCaps& caps,
                 void* stream);
 
 // Kernel-node parameters for a CUDA graph of one step (graph.cu).  The
