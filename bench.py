@@ -65,8 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="per-size kernel measurements (flat 2^20..2^30, latency at 65,536); "
                         "prints one JSON object per size instead of the bench line")
-    p.add_argument("--sweep-latency-only", action="store_true",
-                   help="with --sweep: only the latency case at 65,536")
+    p.add_argument("--sweep-parts", default="sizes,mixed,latency",
+                   help="with --sweep: which parts to run (comma list of sizes, mixed, latency)")
     return p.parse_args(argv)
 
 
@@ -545,7 +545,8 @@ def run_sweep(args):
     peak, peak_kind = measured_peaks()
     flush = torch.ones(128 << 20, device=dev)
     rows = []
-    for log2n in range(20, 31) if not args.sweep_latency_only else ():
+    parts = set(args.sweep_parts.split(","))
+    for log2n in range(20, 31) if "sizes" in parts else ():
         wl = W.flat_pow2(log2n)
         n = wl.n
         w = torch.empty(n, device=dev)
@@ -637,9 +638,10 @@ def run_sweep(args):
         del w, g, m, v
         torch.cuda.empty_cache()
 
-    if not args.sweep_latency_only:
+    if "mixed" in parts:
         sweep_mixed(dev, main, flush, peak)
-    sweep_latency(dev, main)
+    if "latency" in parts:
+        sweep_latency(dev, main)
     return 0
 
 
@@ -664,20 +666,30 @@ def sweep_mixed(dev, main, flush, peak):
     del g32
     w_lp = torch.empty(n, dtype=torch.bfloat16, device=dev)
     with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
-        times = []
-        for t in range(1, 24):
+        times, norm_ms, fused_ms = [], [], []
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in evs:
+            e.record(main)
+        for t in range(1, 44):
             flush.sum()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(main)
+            split = t % 2 == 0  # every other step: an event between the kernels
+            osr.adamw_record_events(ctx, evs[0], evs[1] if split else None, evs[2])
             osr.adamw_clip_step_mixed(ctx, w, g16, m, v, t, wl.lr, wl.wd, wl.clip, w_lp=w_lp)
-            b.record(main)
-            b.synchronize()
+            evs[2].synchronize()
             if t > 3:
-                times.append(a.elapsed_time(b))
+                if split:
+                    norm_ms.append(evs[0].elapsed_time(evs[1]))
+                    fused_ms.append(evs[1].elapsed_time(evs[2]))
+                else:
+                    times.append(evs[0].elapsed_time(evs[2]))
         ms = statistics.median(times)
+        nm, fm = statistics.median(norm_ms), statistics.median(fused_ms)
     row = {"workload": wl.name + " mixed (bf16 g, bf16 weight copy)", "n": n,
            "step": {"ms": ms, "params/s": n / (ms / 1e3), "GB/s": 30 * n / ms / 1e6,
-                    "frac": 30 * n / ms / 1e6 / peak}}
+                    "frac": 30 * n / ms / 1e6 / peak},
+           "k_grad_norm": {"ms": nm, "GB/s": 2 * n / nm / 1e6, "frac": 2 * n / nm / 1e6 / peak},
+           "k_clip_adamw": {"ms": fm, "GB/s": 28 * n / fm / 1e6,
+                            "frac": 28 * n / fm / 1e6 / peak}}
     print(json.dumps(row), flush=True)
     del w, m, v, g16, w_lp
     torch.cuda.empty_cache()
