@@ -155,21 +155,35 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows)}
 
 
-def dist_setup():
+_HOST_GROUP = None  # gloo group for host-side collectives (barrier, max)
+
+
+def dist_setup(device_collectives=False):
+    """Process group from torchrun's environment.  With device_collectives
+    (the GPU arm), the default group is NCCL -- the step's exchange runs on
+    the device -- and a gloo group carries the host-side barrier and max."""
+    global _HOST_GROUP
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("gloo", rank=rank, world_size=world)
+        if device_collectives:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", rank=rank, world_size=world,
+                                    device_id=torch.device("cuda", local))
+            _HOST_GROUP = dist.new_group(backend="gloo")
+        else:
+            dist.init_process_group("gloo", rank=rank, world_size=world)
     return world, rank, local
 
 
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
-        dist.barrier()
+        dist.barrier(group=_HOST_GROUP)
 
 
 def max_over_ranks(x, world):
@@ -178,7 +192,7 @@ def max_over_ranks(x, world):
     import torch
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=_HOST_GROUP)
     return float(t.item())
 
 
@@ -318,7 +332,7 @@ def run_ours(args):
     from synthetic import device as synth_dev
 
     lib_build.build()  # no-op when the library is up to date
-    world, rank, local = dist_setup()
+    world, rank, local = dist_setup(device_collectives=True)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload(args.workload)
@@ -333,6 +347,7 @@ def run_ours(args):
     synth_dev.fill_weights(w, wl.seed)
     synth_dev.fill_grads(g, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
     ctx = osr.adamw_create(n, off, num)
+    exchange = sharded.DeviceExchange(world, dev) if world > 1 else None
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream()
     ckdir = tempfile.mkdtemp(prefix="ckpt_", dir=args.ckpt_dir)
@@ -356,13 +371,15 @@ def run_ours(args):
                 osr.adamw_record_events(ctx, *ev)
             osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
             return
+        # N ranks: the shard's sum of squares, an NCCL all-gather and the
+        # rank-order sum all on the device (no host round trip)
         if ev is not None:
             ev[0].record(main)
-        local = osr.grad_sumsq(ctx, g)
+        osr.grad_sumsq_to(ctx, g, exchange.send)
+        torch.distributed.all_gather_into_tensor(exchange.recv, exchange.send)
         if ev is not None:
             ev[1].record(main)
-        total = sharded.global_sumsq(local)
-        osr.adamw_clip_step_ex(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip, global_sumsq=total)
+        osr.adamw_clip_step_gathered(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip, exchange.recv)
         if ev is not None:
             ev[2].record(main)
 
@@ -467,7 +484,8 @@ def run_ours(args):
         "config": {
             "workload": wl.name, "n_params": n, "tensors": len(off),
             "parallelism": (f"zero1 x{world}: one {wl.name} shard per rank, sums of squares "
-                            f"exchanged (gloo) and added in rank order each step")
+                            f"all-gathered (NCCL, on the device) and added in rank order "
+                            f"each step")
                            if world > 1 else "single GPU",
             "ckpt_every": C, "ckpts_timed": len(ck_steps),
             "ckpt_bytes": 8 + 12 * n,

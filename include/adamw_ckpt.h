@@ -220,6 +220,35 @@ ADAMW_API int grad_sumsq_typed(adamw_ctx* ctx, const void* d_g, int32_t g_dtype,
 ADAMW_API int grad_sumsq(adamw_ctx* ctx, const float* d_g, double* h_sumsq, void* stream);
 
 /*
+ * The sharded step with the exchange on the device ("Checkpoint and Sharded
+ * Resume", lesson 80: each rank holds one contiguous shard; the clip needs
+ * the norm of the whole gradient).  Per step, on each rank, all on `stream`
+ * with no host wait:
+ *   1. grad_sumsq_to: the shard's sum of g^2 (double, the deterministic
+ *      reduction) written to the device address d_out (8-byte aligned) --
+ *      this rank's send buffer of an all-gather;
+ *   2. the caller all-gathers one double per rank into d_rank_sumsq[world]
+ *      in rank order (e.g. an NCCL all-gather on the same stream);
+ *   3. adamw_clip_step_gathered: adds d_rank_sumsq[0..world) in rank order
+ *      on the device, takes grad_scale sqrt(sum) as the norm and the clip
+ *      factor from it -- the same formula and order as adamw_clip_step_ex
+ *      with global_sumsq, so the same bits -- and runs the fused update of
+ *      this rank's shard.  A non-finite sum skips the update (the state is
+ *      left as it was); adamw_last_norm then reports ADAMW_ENONFINITE and
+ *      the global norm.  flags: ADAMW_ZERO_GRAD.
+ * g_dtype: ADAMW_DTYPE_F32 / BF16 / F16 (16-bit: 8-byte aligned; then the
+ * update needs adamw_clip_step_mixed's alignment and takes no weight copy).
+ * Errors: ADAMW_EINVAL (NULL pointers, world < 1, bad scalars), ADAMW_ECUDA.
+ */
+ADAMW_API int grad_sumsq_to(adamw_ctx* ctx, const void* d_g, int32_t g_dtype, double* d_out,
+                            void* stream);
+ADAMW_API int adamw_clip_step_gathered(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype,
+                                       float* d_m, float* d_v, int32_t t, double lr, double wd,
+                                       double clip, double grad_scale,
+                                       const double* d_rank_sumsq, int32_t world, int32_t flags,
+                                       void* stream);
+
+/*
  * One step as a CUDA graph, for states small enough that launch latency
  * dominates (e.g. 65,536 parameters: L2-resident, a few microseconds per
  * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm

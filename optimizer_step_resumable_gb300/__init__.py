@@ -53,6 +53,10 @@ SIGNATURES = {
                                          _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
                                          _c.c_double, _c.c_double, _c.c_int32, _vp]),
     "grad_sumsq_typed": (_c.c_int, [_vp, _vp, _c.c_int32, _c.POINTER(_c.c_double), _vp]),
+    "grad_sumsq_to": (_c.c_int, [_vp, _vp, _c.c_int32, _vp, _vp]),
+    "adamw_clip_step_gathered": (_c.c_int, [_vp, _vp, _vp, _c.c_int32, _vp, _vp, _c.c_int32,
+                                            _c.c_double, _c.c_double, _c.c_double, _c.c_double,
+                                            _vp, _c.c_int32, _c.c_int32, _vp]),
     "adamw_last_tensor_sumsq": (_c.c_int, [_vp, _vp]),
     "adamw_graph_create": (_c.c_int, [_vp, _vp, _vp, _vp, _vp]),
     "adamw_graph_step": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
@@ -297,6 +301,38 @@ def grad_sumsq_typed(ctx: Context, g, stream=None) -> float:
                                     ctypes.byref(out), _stream(stream))
     _check(st, "grad_sumsq_typed")
     return out.value
+
+
+def _f64_dev_ptr(t, k: int, name: str) -> int:
+    import torch
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float64
+            and t.is_contiguous() and t.numel() >= k):
+        raise ValueError(f"{name} must be a contiguous CUDA float64 tensor of >= {k} values")
+    return t.data_ptr()
+
+
+def grad_sumsq_to(ctx: Context, g, out, stream=None):
+    """This shard's sum of g^2 written to the CUDA float64 tensor `out`
+    (its first element) on the stream, with no host wait."""
+    st = library().grad_sumsq_to(ctx.handle, _typed_ptr(g, ctx.n, "g"), _dtype_of(g),
+                                 _f64_dev_ptr(out, 1, "out"), _stream(stream))
+    _check(st, "grad_sumsq_to")
+
+
+def adamw_clip_step_gathered(ctx: Context, w, g, m, v, t: int, lr: float, wd: float,
+                             clip: float, rank_sumsq, grad_scale: float = 1.0,
+                             zero_grad: bool = False, stream=None):
+    """The fused update of this shard with the global norm added up on the
+    device, in rank order, from rank_sumsq (CUDA float64, one value per
+    rank, e.g. the output of an all-gather)."""
+    n = ctx.n
+    world = rank_sumsq.numel()
+    st = library().adamw_clip_step_gathered(
+        ctx.handle, _dev_ptr(w, n, "w"), _typed_ptr(g, n, "g"), _dtype_of(g),
+        _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip),
+        float(grad_scale), _f64_dev_ptr(rank_sumsq, world, "rank_sumsq"), int(world),
+        ZERO_GRAD if zero_grad else 0, _stream(stream))
+    _check(st, "adamw_clip_step_gathered")
 
 
 def grad_tensor_sumsq(ctx: Context, g, stream=None):

@@ -24,8 +24,8 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler",
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall",
              "-I" + INCLUDE]
 
-CUDA_SOURCES = ["norm.cu", "step.cu", "onepass.cu", "pack.cu", "api.cu", "writer.cu",
-                "graph.cu", "noalloc.cu"]
+CUDA_SOURCES = ["norm.cu", "step.cu", "onepass.cu", "ranks.cu", "pack.cu", "api.cu",
+                "writer.cu", "graph.cu", "noalloc.cu"]
 CXX_SOURCES = ["ckpt_io.cpp", "manifest.cpp", "sha256.cpp"]
 
 

@@ -469,10 +469,13 @@ int adamw_clip_step_ex(adamw_ctx* ctx, float* d_w, float* d_g, float* d_m, float
                                  flags, stream);
 }
 
-int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m,
-                          float* d_v, void* d_w_lp, int32_t w_lp_dtype, int32_t t, double lr,
-                          double wd, double clip, double grad_scale, double global_sumsq,
-                          int32_t flags, void* stream)
+// The step behind adamw_clip_step_mixed (and _ex, plain) and
+// adamw_clip_step_gathered (d_rank_sumsq != NULL: the global sum of squares
+// is added up on the device from the ranks' gathered values).
+static int step_impl(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m, float* d_v,
+              void* d_w_lp, int32_t w_lp_dtype, int32_t t, double lr, double wd, double clip,
+              double grad_scale, double global_sumsq, const double* d_rank_sumsq,
+              int32_t world, int32_t flags, void* stream)
 {
     osr::clear_error();
     if (!ctx)
@@ -510,7 +513,12 @@ int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype
         return fail(ADAMW_EINVAL, "grad_scale=%g must be finite and > 0", grad_scale);
     if (flags & ~(ADAMW_ZERO_GRAD | ADAMW_TENSOR_NORMS))
         return fail(ADAMW_EINVAL, "unknown flags 0x%x", flags);
-    const bool external = !(global_sumsq < 0.0);  // NaN counts as given (non-finite)
+    const bool gathered = d_rank_sumsq != nullptr;
+    if (gathered && (world < 1 || (reinterpret_cast<uintptr_t>(d_rank_sumsq) & 7u)))
+        return fail(ADAMW_EINVAL, "world=%d must be >= 1, d_rank_sumsq 8-byte aligned", world);
+    if (gathered && (flags & ADAMW_TENSOR_NORMS))
+        return fail(ADAMW_EINVAL, "per-tensor norms need the shard's own reduction");
+    const bool external = !gathered && !(global_sumsq < 0.0);  // NaN counts as given
 
     osr::StepScalars k = osr::make_step_scalars(ctx, t, lr, wd);
     if (external) {
@@ -532,7 +540,8 @@ int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype
     // the two launches below), also when captured into a graph (a
     // cooperative kernel node); not when an event was asked for between the
     // two kernels.
-    if (!external && g_dtype == ADAMW_DTYPE_F32 && !d_w_lp && !(flags & ADAMW_TENSOR_NORMS) &&
+    if (!external && !gathered && g_dtype == ADAMW_DTYPE_F32 && !d_w_lp &&
+        !(flags & ADAMW_TENSOR_NORMS) &&
         !prof[1] && ctx->onepass && ctx->n <= ctx->onepass_max_n &&
         osr::onepass_grid(ctx->n, ctx->onepass_capacity) <= ctx->onepass_capacity &&
         aligned16(d_w) && aligned16(d_g) && aligned16(d_m) && aligned16(d_v)) {
@@ -544,11 +553,18 @@ int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype
             ctx->onepass_capacity, (flags & ADAMW_ZERO_GRAD) != 0, stream);
         if (e != cudaSuccess)
             return cuda_fail(cudaError_t(e), "one-launch step");
+        ctx->segs_launched = false;  // this reduction wrote no per-tensor sums
         if (prof[2])
             CUDA_TRY(cudaEventRecord(prof[2], st));
         return mark_norm(ctx, st);
     }
-    if (!external) {
+    if (gathered) {
+        const int e = osr::launch_rank_total(d_rank_sumsq, world, clip, grad_scale, ctx->d_res,
+                                             ctx->h_res_dev, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(cudaError_t(e), "global-sum kernel launch");
+        ctx->segs_launched = false;
+    } else if (!external) {
         rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale,
                             (flags & ADAMW_TENSOR_NORMS) != 0, g_dtype);
         if (rc != ADAMW_OK)
@@ -569,6 +585,51 @@ int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype
     if (!external)  // the norm result is complete once the step is
         return mark_norm(ctx, st);
     return ADAMW_OK;
+}
+
+int adamw_clip_step_mixed(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m,
+                          float* d_v, void* d_w_lp, int32_t w_lp_dtype, int32_t t, double lr,
+                          double wd, double clip, double grad_scale, double global_sumsq,
+                          int32_t flags, void* stream)
+{
+    return step_impl(ctx, d_w, d_g, g_dtype, d_m, d_v, d_w_lp, w_lp_dtype, t, lr, wd, clip,
+                     grad_scale, global_sumsq, nullptr, 0, flags, stream);
+}
+
+int adamw_clip_step_gathered(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m,
+                             float* d_v, int32_t t, double lr, double wd, double clip,
+                             double grad_scale, const double* d_rank_sumsq, int32_t world,
+                             int32_t flags, void* stream)
+{
+    osr::clear_error();
+    if (!d_rank_sumsq)
+        return fail(ADAMW_EINVAL, "d_rank_sumsq is NULL");
+    return step_impl(ctx, d_w, d_g, g_dtype, d_m, d_v, nullptr, ADAMW_DTYPE_BF16, t, lr, wd,
+                     clip, grad_scale, -1.0, d_rank_sumsq, world, flags, stream);
+}
+
+int grad_sumsq_to(adamw_ctx* ctx, const void* d_g, int32_t g_dtype, double* d_out, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !d_out || (reinterpret_cast<uintptr_t>(d_out) & 7u))
+        return fail(ADAMW_EINVAL, "ctx is NULL or d_out NULL / not 8-byte aligned");
+    int rc = ADAMW_OK;
+    if (g_dtype == ADAMW_DTYPE_F32)
+        rc = check_state_ptr(d_g, "d_g");
+    else if (g_dtype != ADAMW_DTYPE_BF16 && g_dtype != ADAMW_DTYPE_F16)
+        rc = fail(ADAMW_EINVAL, "g_dtype=%d is not F32, BF16 or F16", g_dtype);
+    else if (!d_g || (reinterpret_cast<uintptr_t>(d_g) & 7u))
+        rc = fail(ADAMW_EINVAL, "a 16-bit d_g must be on an 8-byte boundary");
+    if (rc != ADAMW_OK)
+        return rc;
+    DeviceScope scope(ctx->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = launch_norm_on(ctx, d_g, INFINITY, stream, 1.0, false, g_dtype);
+    if (rc != ADAMW_OK)
+        return rc;
+    CUDA_TRY(cudaMemcpyAsync(d_out, &ctx->d_res->sumsq, sizeof(double), cudaMemcpyDeviceToDevice,
+                             st));
+    return mark_norm(ctx, st);
 }
 
 int grad_tensor_sumsq(adamw_ctx* ctx, const float* d_g, double* h_out, void* stream)

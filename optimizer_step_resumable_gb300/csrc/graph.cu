@@ -235,6 +235,8 @@ int adamw_graph_step(adamw_ctx* ctx, int32_t t, double lr, double wd, double cli
     }
     if (rc == ADAMW_OK && (e = cudaGraphLaunch(ctx->graph_exec, s)) != cudaSuccess)
         rc = osr::cuda_fail(e, "cudaGraphLaunch");
+    if (rc == ADAMW_OK)
+        ctx->segs_launched = false;  // the graph's reduction writes no per-tensor sums
     if (rc == ADAMW_OK) {
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         cudaStreamIsCapturing(s, &cap);

@@ -121,6 +121,10 @@ int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const Step
                    double clip, double grad_scale, double* partials, uint32_t* bar,
                    bool fault_test, NormResult* d_res, NormResult* h_res, int capacity,
                    bool zero_grad, void* stream);
+// The global result of a sharded state from the ranks' gathered sums of
+// squares (ranks.cu): published to d_res / h_res like a norm reduction.
+int launch_rank_total(const double* rank_sumsq, int32_t world, double clip, double grad_scale,
+                      NormResult* d_res, NormResult* h_res, void* stream);
 // States up to this many parameters take the one-launch step by default
 // (measured on GB300: below about 2^20 it saves 2 us per step; from 2^20 up
 // the two launches, which overlap, are faster).

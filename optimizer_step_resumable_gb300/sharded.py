@@ -13,8 +13,8 @@ from __future__ import annotations
 
 import time
 
-from . import (adamw_clip_step_ex, ckpt_manifest_commit, ckpt_pack, ckpt_shard_read,
-               ckpt_shard_write, grad_sumsq)
+from . import (adamw_clip_step_ex, adamw_clip_step_gathered, ckpt_manifest_commit, ckpt_pack,
+               ckpt_shard_read, ckpt_shard_write, grad_sumsq, grad_sumsq_to)
 
 
 def shard_range(n: int, rank: int, world: int, align: int = 4):
@@ -64,6 +64,33 @@ def sharded_clip_step(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=1.0, zero_gra
     adamw_clip_step_ex(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=grad_scale,
                        global_sumsq=total, zero_grad=zero_grad, stream=stream)
     return total
+
+
+class DeviceExchange:
+    """Buffers of the on-device exchange: one float64 to send, one per rank
+    to receive (CUDA tensors, reused every step)."""
+
+    def __init__(self, world: int, device):
+        import torch
+        self.send = torch.zeros(1, dtype=torch.float64, device=device)
+        self.recv = torch.zeros(world, dtype=torch.float64, device=device)
+
+
+def sharded_clip_step_device(ctx, w, g, m, v, t, lr, wd, clip, exchange, grad_scale=1.0,
+                             zero_grad=False, group=None):
+    """One clipped-AdamW step on this rank's shard with no host round trip:
+    the shard's sum of squares goes to exchange.send on the current stream,
+    an all-gather (NCCL: on the device) fills exchange.recv in rank order,
+    and the library adds it up in rank order on the device and updates the
+    shard -- the same bits as sharded_clip_step."""
+    import torch.distributed as dist
+    grad_sumsq_to(ctx, g, exchange.send)
+    if dist.is_available() and dist.is_initialized():
+        dist.all_gather_into_tensor(exchange.recv, exchange.send, group=group)
+    else:
+        exchange.recv.copy_(exchange.send)
+    adamw_clip_step_gathered(ctx, w, g, m, v, t, lr, wd, clip, exchange.recv,
+                             grad_scale=grad_scale, zero_grad=zero_grad)
 
 
 def _gather_objects(obj, group=None):

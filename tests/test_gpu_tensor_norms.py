@@ -128,3 +128,30 @@ def test_step_with_tensor_norms_same_bits(dev, oracle):
         del w, m, v, g
     assert torch.equal(out[0], out[1])
     torch.cuda.empty_cache()
+
+
+def test_small_state_steps_do_not_leave_stale_tensor_sums(dev):
+    """After a step with per-tensor sums, a one-launch step or a graph step
+    (neither computes them) makes adamw_last_tensor_sumsq refuse instead of
+    returning the older step's sums."""
+    sizes = [300, 7, 4000, 1]
+    num = np.array(sizes, np.int64)
+    off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
+    n = int(num.sum())
+    w = torch.zeros(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    g = torch.full((n,), 1e-3, device=dev)
+    with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+        for follow in ("one_launch", "graph"):
+            osr.adamw_clip_step_ex(ctx, w, g, m, v, 1, 1e-3, 0.0, 1.0, tensor_norms=True)
+            assert osr.adamw_last_tensor_sumsq(ctx).shape == (len(sizes),)
+            if follow == "one_launch":
+                osr.adamw_clip_step(ctx, w, g, m, v, 2, 1e-3, 0.0, 1.0)
+            else:
+                osr.adamw_graph_create(ctx, w, g, m, v)
+                osr.adamw_graph_step(ctx, 2, 1e-3, 0.0, 1.0)
+                osr.adamw_graph_destroy(ctx)
+            with pytest.raises(osr.AdamWError) as e:
+                osr.adamw_last_tensor_sumsq(ctx)
+            assert e.value.status == osr.ESTATE
