@@ -39,7 +39,10 @@ def shards(dev, n, world):
 
 @pytest.mark.parametrize("world", [1, 2, 3, 4])
 @pytest.mark.parametrize("n", [65_573, 1_000_003])
-def test_device_exchange_same_bits_as_host_exchange(dev, world, n):
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_device_exchange_same_bits_as_host_exchange(dev, world, n, gdt):
+    if gdt == "bf16" and n != 1_000_003:
+        pytest.skip("one size suffices for the 16-bit gradient")
     runs = []
     for mode in ("host", "device"):
         parts = shards(dev, n, world)
@@ -49,10 +52,12 @@ def test_device_exchange_same_bits_as_host_exchange(dev, world, n):
         for t in (1, 2, 3):
             hg = synthetic.grads(7, t, 1e-2, n=n, outlier_frac=0.01, outlier_mult=100.0)
             gs = [torch.from_numpy(hg[off:off + num].copy()).to(dev) for off, num, _ in parts]
+            if gdt == "bf16":
+                gs = [g.to(torch.bfloat16) for g in gs]
             if mode == "host":
-                total = sharded.ordered_sum(osr.grad_sumsq(c, g) for c, g in zip(ctxs, gs))
+                total = sharded.ordered_sum(osr.grad_sumsq_typed(c, g) for c, g in zip(ctxs, gs))
                 for c, (_, _, (w, m, v)), g in zip(ctxs, parts, gs):
-                    osr.adamw_clip_step_ex(c, w, g, m, v, t, LR, WD, CLIP, global_sumsq=total)
+                    osr.adamw_clip_step_mixed(c, w, g, m, v, t, LR, WD, CLIP, global_sumsq=total)
             else:
                 for r, (c, g) in enumerate(zip(ctxs, gs)):
                     osr.grad_sumsq_to(c, g, recv[r:r + 1])
