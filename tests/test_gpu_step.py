@@ -317,3 +317,28 @@ def test_step_is_bit_stable(dev):
                 osr.adamw_clip_step(ctx, w, g, m, v, t, 3e-3, 0.01, 1.0)
         res.append(torch.cat([w, m, v]).cpu())
     assert torch.equal(res[0], res[1]) and torch.equal(res[0], res[2])
+
+
+@pytest.mark.parametrize("flags", [0, osr.LAUNCH_NO_ONEPASS])
+def test_clip_threshold_is_strict(dev, flags):
+    """g = [0.375, 0.5] has norm exactly 0.625 (exact squares and root).
+    c = 0.625: no clip (the comparison is strict), factor exactly 1.
+    c = 0.625 (1 - 2^-24): clipped, factor c / norm = 1 - 2^-24 exactly, the
+    largest float below 1.  (One double below 0.625 also clips, but its
+    factor 1 - 2^-53 rounds to 1.0f: the factor is a float.)"""
+    g = torch.tensor([0.375, 0.5, 0.0, 0.0], device=dev)
+    below = 0.625 * (1.0 - 2.0 ** -24)
+    for clip, want_scale in ((0.625, 1.0), (below, float(np.float32(1.0 - 2.0 ** -24))),
+                             (np.nextafter(0.625, 0.0), 1.0)):
+        w = torch.tensor([1.0, -1.0, 0.5, 2.0], device=dev)
+        m = torch.zeros(4, device=dev)
+        v = torch.zeros(4, device=dev)
+        with osr.adamw_create(4, flags=osr.CREATE_NO_CKPT) as ctx:
+            osr.adamw_set_launch_options(ctx, flags)
+            osr.adamw_clip_step(ctx, w, g, m, v, 1, 1e-3, 0.0, float(clip))
+            norm, scale = osr.adamw_last_norm(ctx)
+        assert norm == 0.625
+        assert scale == want_scale, (clip, scale)
+        # m = (1 - beta1) * (g s), one float32 rounding of each product
+        gh = np.float32(np.float32(0.5) * np.float32(want_scale))
+        assert m.cpu().numpy()[1] == np.float32(np.float32(0.1) * gh)
