@@ -588,14 +588,18 @@ def ckpt_manifest_commit(directory: str, step: int, offsets, numels, digests,
 
 def ckpt_manifest_load(step_dir: str, expected_world: int = -1, verify: bool = True):
     """(step, offsets, numels) of a validated sharded checkpoint."""
-    cap = 4096
+    lib = library()
+    step, world = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    # the shard count first (no digests), then the table at its size
+    st = lib.ckpt_manifest_load(os.fsencode(step_dir), int(expected_world), 0,
+                                ctypes.byref(step), ctypes.byref(world), None, None, 0)
+    _check(st, "ckpt_manifest_load")
+    cap = max(1, world.value)
     po = (ctypes.c_int64 * cap)()
     pn = (ctypes.c_int64 * cap)()
-    step, world = ctypes.c_int32(-1), ctypes.c_int32(-1)
-    st = library().ckpt_manifest_load(os.fsencode(step_dir), int(expected_world),
-                                      1 if verify else 0, ctypes.byref(step),
-                                      ctypes.byref(world), ctypes.addressof(po),
-                                      ctypes.addressof(pn), cap)
+    st = lib.ckpt_manifest_load(os.fsencode(step_dir), int(expected_world), 1 if verify else 0,
+                                ctypes.byref(step), ctypes.byref(world), ctypes.addressof(po),
+                                ctypes.addressof(pn), cap)
     _check(st, "ckpt_manifest_load")
     return step.value, list(po[:world.value]), list(pn[:world.value])
 
