@@ -32,8 +32,10 @@
  *    are accepted and take a scalar path.
  *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls are asynchronous on that stream unless stated.
- *  - The context owns all scratch (device, pinned host); nothing is
- *    allocated after adamw_create.
+ *  - The context owns all scratch (device, pinned host), allocated by
+ *    adamw_create; the only later allocations are made by setup calls
+ *    outside the training loop (adamw_set_decay_mask: the flag bits;
+ *    adamw_graph_create: the step graph).  No step allocates.
  *  - A context is not thread-safe: one host thread drives it at a time.
  */
 #ifndef ADAMW_CKPT_H
