@@ -35,7 +35,8 @@
  *  - The context owns all scratch (device, pinned host), allocated by
  *    adamw_create; the only later allocations are made by setup calls
  *    outside the training loop (adamw_set_decay_mask: the flag bits;
- *    adamw_graph_create: the step graph).  No step allocates.
+ *    adamw_graph_create: the step graph).  No step allocates, except the
+ *    first graph step after such a setup change, which rebuilds its graph.
  *  - A context is not thread-safe: one host thread drives it at a time.
  */
 #ifndef ADAMW_CKPT_H
