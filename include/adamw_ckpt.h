@@ -78,6 +78,7 @@ extern "C" {
 #define ADAMW_LAUNCH_NO_PDL 1     /* launch the fused kernel after the norm ends */
 #define ADAMW_LAUNCH_NO_ONEPASS 2 /* small states: two launches, not one         */
 #define ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT 4 /* tests only: see below          */
+#define ADAMW_LAUNCH_STATIC_CHUNKS 8 /* fused kernel: chunks fixed per block    */
 
 /* adamw_clip_step_ex flags. */
 #define ADAMW_ZERO_GRAD 1    /* write 0 into g after reading it             */
@@ -85,6 +86,7 @@ extern "C" {
 
 /* ckpt_set_options / ckpt_write_image flags. */
 #define CKPT_DIRECT 1 /* write with O_DIRECT when the file system allows it */
+#define CKPT_COPY_ENGINE 2 /* staging -> host image by the copy engine       */
 
 /* Checkpoint requests recorded by the signal handlers (ckpt_signals_*). */
 #define CKPT_REQ_WRITE 1 /* SIGUSR1: write a checkpoint, keep training     */
@@ -361,8 +363,11 @@ ADAMW_API int adamw_record_events(adamw_ctx* ctx, void* ev_begin, void* ev_mid,
 /*
  * Checkpoint, part 1 ([C] "Format"; [T] "save after a complete optimizer
  * step"): a kernel on main_stream packs [int32 step][int32 n][w][m][v] into
- * the context's device staging image (8 + 12 n bytes, little-endian), then
- * side_stream copies that image into the context's pinned host image.  The
+ * the context's device staging (the header and the w, m, v regions, little-
+ * endian, each in a 256-byte aligned slot), then side_stream copies them to
+ * their file offsets in the context's pinned host image (8 + 12 n bytes):
+ * by a kernel of one block per SM by default, by the copy engine with
+ * CKPT_COPY_ENGINE (see ckpt_set_options).  The
  * caller may launch the next step on main_stream right away: the pack reads
  * w, m, v before it, and the copy reads only the staging image.  A later
  * pack waits for the previous copy.  side_stream may equal main_stream.
@@ -404,7 +409,13 @@ ADAMW_API int ckpt_wait(adamw_ctx* ctx, char* path_out, size_t path_cap);
  * Writer options: keep >= 1 keeps only the newest `keep` step_*.bin files of
  * the target directory after each write ([S] "Production patterns": rotation
  * keeps the last K checkpoints so the disk does not fill); keep = 0 keeps
- * all.  flags: CKPT_DIRECT or 0.  Defaults: keep = 0, CKPT_DIRECT.
+ * all.  flags: CKPT_DIRECT, CKPT_COPY_ENGINE, both or 0.  Defaults:
+ * keep = 0, CKPT_DIRECT.  CKPT_COPY_ENGINE makes ckpt_pack copy the staging
+ * to the pinned image with the copy engine instead of a kernel on the side
+ * stream: the copy engine leaves the SMs to the steps running meanwhile,
+ * but on GB300 its copy into a pinned image that was just written to a file
+ * took 80-116 ms for 1.33 GB where the kernel took 7-14 ms (and the steps
+ * lost about 4 ms); the write of the next checkpoint waits for that copy.
  */
 ADAMW_API int ckpt_set_options(adamw_ctx* ctx, int32_t keep, int32_t flags);
 

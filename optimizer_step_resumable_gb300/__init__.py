@@ -21,12 +21,14 @@ OK = 0
 EINVAL, ECUDA, EIO, EFORMAT, ESIZE, EMISMATCH, ENONFINITE, ESTATE = range(-1, -9, -1)
 CREATE_NO_CKPT = 1
 CKPT_DIRECT = 1
+CKPT_COPY_ENGINE = 2
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 ZERO_GRAD = 1
 TENSOR_NORMS = 2
 LAUNCH_NO_PDL = 1
 LAUNCH_NO_ONEPASS = 2
 LAUNCH_TEST_BARRIER_TIMEOUT = 4
+LAUNCH_STATIC_CHUNKS = 8
 CKPT_REQ_WRITE, CKPT_REQ_EXIT = 1, 2
 CKPT_ACTION_NONE, CKPT_ACTION_WRITING, CKPT_ACTION_EXIT = 0, 1, 2
 

@@ -101,7 +101,23 @@ __device__ __forceinline__ void vector_pass(float* __restrict__ w, const G* __re
         const int64_t n4 = n >> 2;
         constexpr int64_t chunk = int64_t(kStepThreads) * kStepVec;
         const int64_t nchunks = n4 / chunk;
-        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        // Chunks: handed out by an atomic counter when k.chunk_ctr is set --
+        // a block that starts late (its SM busy with another kernel) simply
+        // takes fewer -- else dealt out cyclically by block.  Thread 0 asks
+        // for the block's next chunk while the current one is processed.
+        __shared__ uint32_t s_next[2];
+        uint32_t* const ctr = k.chunk_ctr;
+        int buf = 0;
+        int64_t c = blockIdx.x;
+        if (ctr) {
+            if (threadIdx.x == 0)
+                s_next[0] = atomicAdd(ctr, 1u);
+            __syncthreads();
+            c = s_next[0];
+        }
+        while (c < nchunks) {
+            if (ctr && threadIdx.x == 0)
+                s_next[buf ^ 1] = atomicAdd(ctr, 1u);
             const int64_t i0 = c * chunk + threadIdx.x;
             float4 W[kStepVec], G4[kStepVec], M[kStepVec], V[kStepVec];
             uint32_t D[kStepVec];
@@ -127,6 +143,22 @@ __device__ __forceinline__ void vector_pass(float* __restrict__ w, const G* __re
                     detail::store4_zero_cs(gw + (i << 2));
                 if constexpr (kCopy)
                     detail::store4_lp_cs(w_lp + (i << 2), W[j]);
+            }
+            if (ctr) {
+                __syncthreads();  // the prefetched index is visible; s_next[buf] is free
+                buf ^= 1;
+                c = s_next[buf];
+            } else {
+                c += gridDim.x;
+            }
+        }
+        if (ctr && threadIdx.x == 0) {
+            // every block has drawn its last index before it counts itself
+            // out; the last one out resets the counters for the next launch
+            __threadfence();
+            if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+                atomicExch(ctr, 0u);
+                atomicExch(ctr + 1, 0u);
             }
         }
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {

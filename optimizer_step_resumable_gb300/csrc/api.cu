@@ -218,6 +218,7 @@ StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double w
     k.decay = float(1.0 - lr * wd);
     k.scale = 1.0f;
     k.decay_mask = c->decay_mask_on ? c->d_decay_mask : nullptr;
+    k.chunk_ctr = c->dynamic_chunks ? c->d_chunk_ctr : nullptr;
     return k;
 }
 
@@ -294,7 +295,8 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
     c->d_res = reinterpret_cast<osr::NormResult*>(c->d_scratch);
     c->d_counter = reinterpret_cast<unsigned int*>(c->d_scratch + sizeof(osr::NormResult));
     c->d_bar = reinterpret_cast<uint32_t*>(c->d_scratch + 64);
-    static_assert(sizeof(osr::NormResult) + sizeof(unsigned int) <= 64 && 64 + 8 <= kScratchHead,
+    c->d_chunk_ctr = reinterpret_cast<uint32_t*>(c->d_scratch + 72);
+    static_assert(sizeof(osr::NormResult) + sizeof(unsigned int) <= 64 && 72 + 8 <= kScratchHead,
                   "scratch head layout");
     c->d_partials = reinterpret_cast<double*>(c->d_scratch + kScratchHead);
     if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_res), sizeof(osr::NormResult),
@@ -356,10 +358,13 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
             return bail(cuda_fail(e, "cudaMalloc(checkpoint staging)"));
         }
         if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_image_alloc),
-                               c->h_image_capacity(), cudaHostAllocDefault)) != cudaSuccess) {
+                               c->h_image_capacity(), cudaHostAllocMapped)) != cudaSuccess) {
             c->h_image_alloc = nullptr;
             return bail(cuda_fail(e, "cudaHostAlloc(checkpoint image)"));
         }
+        if ((e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->h_image_dev),
+                                          c->h_image_alloc, 0)) != cudaSuccess)
+            return bail(cuda_fail(e, "cudaHostGetDevicePointer(checkpoint image)"));
         if ((e = cudaEventCreateWithFlags(&c->ev_pack, cudaEventDisableTiming)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&c->ev_d2h, cudaEventDisableTiming)) != cudaSuccess)
             return bail(cuda_fail(e, "cudaEventCreate"));
@@ -666,8 +671,10 @@ int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags)
     osr::clear_error();
     if (!ctx)
         return fail(ADAMW_EINVAL, "ctx is NULL");
-    if (flags & ~(ADAMW_LAUNCH_NO_PDL | ADAMW_LAUNCH_NO_ONEPASS | ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT))
+    if (flags & ~(ADAMW_LAUNCH_NO_PDL | ADAMW_LAUNCH_NO_ONEPASS |
+                  ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT | ADAMW_LAUNCH_STATIC_CHUNKS))
         return fail(ADAMW_EINVAL, "unknown launch flags 0x%x", flags);
+    ctx->dynamic_chunks = !(flags & ADAMW_LAUNCH_STATIC_CHUNKS);
     ctx->pdl = !(flags & ADAMW_LAUNCH_NO_PDL);
     ctx->onepass = !(flags & ADAMW_LAUNCH_NO_ONEPASS);
     ctx->onepass_fault_test = (flags & ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT) != 0;
@@ -758,11 +765,22 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
     if (side != mainst)
         CUDA_TRY(cudaStreamWaitEvent(side, ctx->ev_pack, 0));
     // the header and the three regions to their file offsets in the image
-    const size_t rb = size_t(4) * size_t(ctx->n);
-    CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_stage(0), 8, cudaMemcpyDeviceToHost, side));
-    for (int r = 1; r <= 3; ++r)
-        CUDA_TRY(cudaMemcpyAsync(ctx->h_image() + 8 + size_t(r - 1) * rb, ctx->d_stage(r), rb,
-                                 cudaMemcpyDeviceToHost, side));
+    if (ctx->copy_engine) {
+        const size_t rb = size_t(4) * size_t(ctx->n);
+        CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_stage(0), 8, cudaMemcpyDeviceToHost,
+                                 side));
+        for (int r = 1; r <= 3; ++r)
+            CUDA_TRY(cudaMemcpyAsync(ctx->h_image() + 8 + size_t(r - 1) * rb, ctx->d_stage(r),
+                                     rb, cudaMemcpyDeviceToHost, side));
+    } else {
+        const int ce = osr::launch_stage_to_host(
+            ctx->d_stage(0), reinterpret_cast<const float*>(ctx->d_stage(1)),
+            reinterpret_cast<const float*>(ctx->d_stage(2)),
+            reinterpret_cast<const float*>(ctx->d_stage(3)), ctx->n, ctx->h_image_dev,
+            ctx->sm_count, side);
+        if (ce != cudaSuccess)
+            return cuda_fail(cudaError_t(ce), "staging copy kernel launch");
+    }
     CUDA_TRY(cudaEventRecord(ctx->ev_d2h, side));
     ctx->packed = true;
     ctx->d2h_pending = true;

@@ -41,7 +41,8 @@ struct adamw_ctx {
     osr::KernelCaps caps{};
     double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
 
-    // norm scratch: [NormResult | counter | barrier x 2 | pad][partials x kNormBlocksMax]
+    // norm scratch: [NormResult | counter | barrier x 2 | chunk counters x 2 | pad]
+    //               [partials x kNormBlocksMax]
     unsigned char* d_scratch = nullptr;
     osr::NormResult* d_res = nullptr;
     unsigned int* d_counter = nullptr;
@@ -68,6 +69,8 @@ struct adamw_ctx {
     // the barrier timeout.
     int onepass_capacity = 0;
     uint32_t* d_bar = nullptr;
+    uint32_t* d_chunk_ctr = nullptr;  // the fused kernel's chunk counters
+    bool dynamic_chunks = true;
     bool onepass = true;
     int64_t onepass_max_n = 0;
     bool onepass_fault_test = false;
@@ -104,6 +107,8 @@ struct adamw_ctx {
     // Checkpoint writing: options and the writer thread.
     int32_t keep = 0;                   // rotation: newest files kept (0 = all)
     int32_t write_flags = osr::kWriteDirect;
+    bool copy_engine = false;  // staging -> host by cudaMemcpyAsync, not the SM kernel
+    unsigned char* h_image_dev = nullptr;  // device address of the pinned host image
     osr::WriterState writer;
 
     static constexpr size_t kStageAlign = 256;

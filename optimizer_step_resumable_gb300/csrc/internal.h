@@ -45,6 +45,10 @@ struct StepScalars {
     // Per-element decay flags (bit e % 32 of word e / 32 set: element e
     // decays); NULL: every element decays.
     const uint32_t* decay_mask;
+    // Dynamic chunk scheduling of the fused kernel: [0] the next chunk to
+    // hand out, [1] blocks done (both 0 between launches: the last block
+    // out resets them).  NULL: chunks are dealt out cyclically by block.
+    uint32_t* chunk_ctr;
 };
 
 // Tunables of the kernels (fixed at compile time; used in norm.cu, step.cu).
@@ -121,6 +125,11 @@ int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const Step
                    double clip, double grad_scale, double* partials, uint32_t* bar,
                    bool fault_test, NormResult* d_res, NormResult* h_res, int capacity,
                    bool zero_grad, void* stream);
+// Staging slots -> the pinned host image (its device address), by the SMs:
+// header (8 bytes) then w, m, v at their file offsets.
+int launch_stage_to_host(const unsigned char* header, const float* sw, const float* sm,
+                         const float* sv, int64_t n, unsigned char* image_dev, int blocks,
+                         void* stream);
 // The global result of a sharded state from the ranks' gathered sums of
 // squares (ranks.cu): published to d_res / h_res like a norm reduction.
 int launch_rank_total(const double* rank_sumsq, int32_t world, double clip, double grad_scale,

@@ -138,6 +138,7 @@ extern "C" int adamw_clip_step_noalloc(float* d_w, const float* d_g, float* d_m,
     k.decay = float(1.0 - lr * wd);
     k.scale = 1.0f;  // unused: the factor comes from the norm result
     k.decay_mask = nullptr;  // decay on every parameter
+    k.chunk_ctr = nullptr;   // chunks dealt out cyclically (no counter scratch)
 
     int le = osr::launch_norm(d_g, n, clip, partials, counter, res, nullptr, stream);
     if (le != cudaSuccess)

@@ -163,11 +163,12 @@ int ckpt_set_options(adamw_ctx* ctx, int32_t keep, int32_t flags)
     osr::clear_error();
     if (!ctx)
         return osr::fail(ADAMW_EINVAL, "ctx is NULL");
-    if (keep < 0 || (flags & ~CKPT_DIRECT))
+    if (keep < 0 || (flags & ~(CKPT_DIRECT | CKPT_COPY_ENGINE)))
         return osr::fail(ADAMW_EINVAL, "keep=%d must be >= 0; unknown flags 0x%x", keep, flags);
     osr::writer_drain(ctx);
     ctx->keep = keep;
     ctx->write_flags = (flags & CKPT_DIRECT) ? osr::kWriteDirect : 0;
+    ctx->copy_engine = (flags & CKPT_COPY_ENGINE) != 0;
     return ADAMW_OK;
 }
 

@@ -31,10 +31,17 @@ def state(dev, n, seed=7):
     return [torch.from_numpy(h).to(dev) for h in (hw, hm, hv)], (hw, hm, hv)
 
 
-@pytest.mark.parametrize("n", [1, 3, 4, 5, 1001, 65536, 65536 + 2])
-def test_pack_write_bytes_match_oracle(dev, oracle, tmp_path, n):
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 6, 7, 1001, 65536, 65536 + 2, 1_000_003])
+@pytest.mark.parametrize("copy", ["kernel", "copy_engine"])
+def test_pack_write_bytes_match_oracle(dev, oracle, tmp_path, n, copy):
+    """Both ways from the staging to the pinned image (the side-stream
+    kernel, whose host stores follow the regions' alignment -- 16, 8 or 4
+    bytes for n % 4 = 0, 2, odd -- and the copy engine) give the oracle's
+    bytes."""
     (w, m, v), hstate = state(dev, n)
     with osr.adamw_create(n) as ctx:
+        osr.ckpt_set_options(ctx, 0, osr.CKPT_DIRECT | (osr.CKPT_COPY_ENGINE
+                                                         if copy == "copy_engine" else 0))
         side = torch.cuda.Stream()
         osr.ckpt_pack(ctx, 80, w, m, v, side_stream=side)
         path = osr.ckpt_write(ctx, str(tmp_path))

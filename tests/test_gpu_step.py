@@ -342,3 +342,31 @@ def test_clip_threshold_is_strict(dev, flags):
         # m = (1 - beta1) * (g s), one float32 rounding of each product
         gh = np.float32(np.float32(0.5) * np.float32(want_scale))
         assert m.cpu().numpy()[1] == np.float32(np.float32(0.1) * gh)
+
+
+@pytest.mark.parametrize("which", ["gpt-110M-list", "flat-2^27+5"])
+def test_dynamic_chunks_same_bits_as_static(dev, which):
+    """The fused kernel hands chunks out by an atomic counter; every element
+    is updated exactly once, so the whole state equals, bit for bit, the
+    state after the same steps with chunks fixed per block (a skipped or
+    repeated chunk would differ)."""
+    n = W.gpt_110m().n if which == "gpt-110M-list" else (1 << 27) + 5
+    outs = []
+    for flags in (0, osr.LAUNCH_STATIC_CHUNKS):
+        (w, m, v), _ = make_state(dev, n, m_sigma=1e-3, v_sigma=1e-5)
+        g = torch.empty(n, device=dev)
+        with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+            osr.adamw_set_launch_options(ctx, flags)
+            for t in (1, 2, 3):
+                synth_dev.fill_grads(g, 7, t, 1e-3, 0.001, 1000.0)
+                osr.adamw_clip_step_ex(ctx, w, g, m, v, t, 3e-3, 0.01, 1.0, zero_grad=(t == 3))
+            torch.cuda.synchronize()
+        outs.append([hashlib_digest(x) for x in (w, m, v, g)])
+        del w, m, v, g
+        torch.cuda.empty_cache()
+    assert outs[0] == outs[1]
+
+
+def hashlib_digest(t):
+    import hashlib
+    return hashlib.sha256(t.cpu().numpy().tobytes()).hexdigest()
