@@ -296,7 +296,8 @@ int adamw_create(int64_t n_params, const int64_t* offsets, const int64_t* numels
     c->d_counter = reinterpret_cast<unsigned int*>(c->d_scratch + sizeof(osr::NormResult));
     c->d_bar = reinterpret_cast<uint32_t*>(c->d_scratch + 64);
     c->d_chunk_ctr = reinterpret_cast<uint32_t*>(c->d_scratch + 72);
-    static_assert(sizeof(osr::NormResult) + sizeof(unsigned int) <= 64 && 72 + 8 <= kScratchHead,
+    c->d_pack_ctr = reinterpret_cast<uint32_t*>(c->d_scratch + 80);
+    static_assert(sizeof(osr::NormResult) + sizeof(unsigned int) <= 64 && 80 + 8 <= kScratchHead,
                   "scratch head layout");
     c->d_partials = reinterpret_cast<double*>(c->d_scratch + kScratchHead);
     if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_res), sizeof(osr::NormResult),
@@ -758,7 +759,7 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
                                    reinterpret_cast<float*>(ctx->d_stage(1)),
                                    reinterpret_cast<float*>(ctx->d_stage(2)),
                                    reinterpret_cast<float*>(ctx->d_stage(3)), ctx->caps,
-                                   main_stream);
+                                   main_stream, ctx->dynamic_chunks ? ctx->d_pack_ctr : nullptr);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "pack kernel launch");
     CUDA_TRY(cudaEventRecord(ctx->ev_pack, mainst));

@@ -41,7 +41,8 @@ struct adamw_ctx {
     osr::KernelCaps caps{};
     double beta1 = 0.9, beta2 = 0.999, eps = 1e-8;
 
-    // norm scratch: [NormResult | counter | barrier x 2 | chunk counters x 2 | pad]
+    // norm scratch: [NormResult | counter | barrier x 2 | chunk counters x 2 |
+    //                pack counters x 2 | pad]
     //               [partials x kNormBlocksMax]
     unsigned char* d_scratch = nullptr;
     osr::NormResult* d_res = nullptr;
@@ -70,6 +71,7 @@ struct adamw_ctx {
     int onepass_capacity = 0;
     uint32_t* d_bar = nullptr;
     uint32_t* d_chunk_ctr = nullptr;  // the fused kernel's chunk counters
+    uint32_t* d_pack_ctr = nullptr;   // the pack kernel's (its own: it may run on another stream)
     bool dynamic_chunks = true;
     bool onepass = true;
     int64_t onepass_max_n = 0;

@@ -142,7 +142,7 @@ constexpr int64_t kOnePassMaxN = int64_t(1) << 19;
 // (16-byte aligned; 256-byte aligned for full speed) of the staging buffer.
 int launch_pack(const float* w, const float* m, const float* v, int64_t n, int32_t step,
                 unsigned char* header, float* dw, float* dm, float* dv, const KernelCaps& caps,
-                void* stream);
+                void* stream, uint32_t* chunk_ctr = nullptr);
 
 // Kernel-node parameters for a CUDA graph of one step (graph.cu).  The
 // argument structs own the values that kernelParams point into.

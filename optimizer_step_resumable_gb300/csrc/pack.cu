@@ -29,11 +29,15 @@ constexpr int kPackThreads = 256;
 constexpr int kPackVec = 2;           // float4 of each array per thread per chunk
 constexpr int kPackBlocksPerSm = 8;   // measured best: two rounds of resident blocks
 
+// ctr (may be NULL): chunk counters as in the fused kernel (handed out by an
+// atomic counter, reset by the last block out); NULL: chunks dealt out
+// cyclically by block.
 template <bool kVec>
 __global__ void __launch_bounds__(kPackThreads, 4)
     k_ckpt_pack(const float* __restrict__ w, const float* __restrict__ m,
                 const float* __restrict__ v, int64_t n, int32_t step, int2* __restrict__ header,
-                float* __restrict__ dw, float* __restrict__ dm, float* __restrict__ dv)
+                float* __restrict__ dw, float* __restrict__ dm, float* __restrict__ dv,
+                uint32_t* __restrict__ ctr)
 {
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *header = make_int2(step, int32_t(n));
@@ -50,7 +54,18 @@ __global__ void __launch_bounds__(kPackThreads, 4)
         const int64_t n4 = n >> 2;
         constexpr int64_t chunk = int64_t(kPackThreads) * kPackVec;
         const int64_t nchunks = n4 / chunk;
-        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        __shared__ uint32_t s_next[2];
+        int buf = 0;
+        int64_t c = blockIdx.x;
+        if (ctr) {
+            if (threadIdx.x == 0)
+                s_next[0] = atomicAdd(ctr, 1u);
+            __syncthreads();
+            c = s_next[0];
+        }
+        while (c < nchunks) {
+            if (ctr && threadIdx.x == 0)
+                s_next[buf ^ 1] = atomicAdd(ctr, 1u);
             const int64_t i0 = c * chunk + threadIdx.x;
             float4 a[kPackVec], b[kPackVec], e[kPackVec];
 #pragma unroll
@@ -64,6 +79,20 @@ __global__ void __launch_bounds__(kPackThreads, 4)
                 __stcs(dw4 + i0 + j * kPackThreads, a[j]);
                 __stcs(dm4 + i0 + j * kPackThreads, b[j]);
                 __stcs(dv4 + i0 + j * kPackThreads, e[j]);
+            }
+            if (ctr) {
+                __syncthreads();
+                buf ^= 1;
+                c = s_next[buf];
+            } else {
+                c += gridDim.x;
+            }
+        }
+        if (ctr && threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+                atomicExch(ctr, 0u);
+                atomicExch(ctr + 1, 0u);
             }
         }
         for (int64_t i = nchunks * chunk + gtid; i < n4; i += stride) {
@@ -158,7 +187,7 @@ int query_pack_caps(int sm_count, KernelCaps* caps)
 
 int launch_pack(const float* w, const float* m, const float* v, int64_t n, int32_t step,
                 unsigned char* header, float* dw, float* dm, float* dv, const KernelCaps& caps,
-                void* stream)
+                void* stream, uint32_t* chunk_ctr)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int2* h = reinterpret_cast<int2*>(header);
@@ -166,12 +195,14 @@ int launch_pack(const float* w, const float* m, const float* v, int64_t n, int32
         const int cap = caps.pack_vec;
         const int64_t want = detail::ceil_div(n >> 2, int64_t(kPackThreads) * kPackVec);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        k_ckpt_pack<true><<<blocks, kPackThreads, 0, s>>>(w, m, v, n, step, h, dw, dm, dv);
+        k_ckpt_pack<true><<<blocks, kPackThreads, 0, s>>>(w, m, v, n, step, h, dw, dm, dv,
+                                                          chunk_ctr);
     } else {
         const int cap = caps.pack_scalar;
         const int64_t want = detail::ceil_div(n, kPackThreads);
         const int blocks = int(want < 1 ? 1 : (want > cap ? cap : want));
-        k_ckpt_pack<false><<<blocks, kPackThreads, 0, s>>>(w, m, v, n, step, h, dw, dm, dv);
+        k_ckpt_pack<false><<<blocks, kPackThreads, 0, s>>>(w, m, v, n, step, h, dw, dm, dv,
+                                                           nullptr);
     }
     return int(cudaGetLastError());
 }
