@@ -78,7 +78,7 @@ extern "C" {
 #define ADAMW_LAUNCH_NO_PDL 1     /* launch the fused kernel after the norm ends */
 #define ADAMW_LAUNCH_NO_ONEPASS 2 /* small states: two launches, not one         */
 #define ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT 4 /* tests only: see below          */
-#define ADAMW_LAUNCH_STATIC_CHUNKS 8 /* fused kernel: chunks fixed per block    */
+#define ADAMW_LAUNCH_STATIC_CHUNKS 8 /* fused, pack: chunks fixed per block     */
 
 /* adamw_clip_step_ex flags. */
 #define ADAMW_ZERO_GRAD 1    /* write 0 into g after reading it             */
@@ -344,6 +344,11 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * wait is bounded (about one second); a wait that runs out skips the update
  * and makes the next adamw_last_norm return ADAMW_ECUDA.
  * ADAMW_LAUNCH_NO_ONEPASS always uses the two launches.
+ * From 2^24 parameters up, the fused kernel and the checkpoint pack hand
+ * their chunks out by an atomic counter, so a block that starts late (its
+ * SM held by other work) takes fewer and no block's share sets the kernel's
+ * end; the results are the same bits.  ADAMW_LAUNCH_STATIC_CHUNKS deals
+ * chunks out cyclically by block at every size.
  * ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT (for tests of that path): the next
  * one-launch step waits for one block more than it launched, so its barrier
  * runs out after about a second, as above.  Used once, then cleared.

@@ -218,7 +218,7 @@ StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double w
     k.decay = float(1.0 - lr * wd);
     k.scale = 1.0f;
     k.decay_mask = c->decay_mask_on ? c->d_decay_mask : nullptr;
-    k.chunk_ctr = c->dynamic_chunks ? c->d_chunk_ctr : nullptr;
+    k.chunk_ctr = (c->dynamic_chunks && c->n >= kDynamicChunksMinN) ? c->d_chunk_ctr : nullptr;
     return k;
 }
 
@@ -759,7 +759,10 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
                                    reinterpret_cast<float*>(ctx->d_stage(1)),
                                    reinterpret_cast<float*>(ctx->d_stage(2)),
                                    reinterpret_cast<float*>(ctx->d_stage(3)), ctx->caps,
-                                   main_stream, ctx->dynamic_chunks ? ctx->d_pack_ctr : nullptr);
+                                   main_stream,
+                                   (ctx->dynamic_chunks && ctx->n >= osr::kDynamicChunksMinN)
+                                       ? ctx->d_pack_ctr
+                                       : nullptr);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "pack kernel launch");
     CUDA_TRY(cudaEventRecord(ctx->ev_pack, mainst));

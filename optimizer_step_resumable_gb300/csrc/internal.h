@@ -134,6 +134,11 @@ int launch_stage_to_host(const unsigned char* header, const float* sw, const flo
 // squares (ranks.cu): published to d_res / h_res like a norm reduction.
 int launch_rank_total(const double* rank_sumsq, int32_t world, double clip, double grad_scale,
                       NormResult* d_res, NormResult* h_res, void* stream);
+// Chunks are handed out by a counter (fused and pack kernels) from this many
+// parameters up (measured on GB300: +3-8% from 2^24, where a block gets 13
+// chunks or more; below, the counter's atomics and block barriers cost more
+// than the balance saves, e.g. 0.86 vs 0.96 of peak at 2^22).
+constexpr int64_t kDynamicChunksMinN = int64_t(1) << 24;
 // States up to this many parameters take the one-launch step by default
 // (measured on GB300: below about 2^20 it saves 2 us per step; from 2^20 up
 // the two launches, which overlap, are faster).
