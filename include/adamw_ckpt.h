@@ -371,8 +371,9 @@ ADAMW_API int adamw_record_events(adamw_ctx* ctx, void* ev_begin, void* ev_mid,
  * the context's device staging (the header and the w, m, v regions, little-
  * endian, each in a 256-byte aligned slot), then side_stream copies them to
  * their file offsets in the context's pinned host image (8 + 12 n bytes):
- * by a kernel of one block per SM by default, by the copy engine with
- * CKPT_COPY_ENGINE (see ckpt_set_options).  The
+ * by a kernel on a quarter of the SMs by default (aligned 16-byte stores
+ * into host memory), by the copy engine with CKPT_COPY_ENGINE (see
+ * ckpt_set_options).  The
  * caller may launch the next step on main_stream right away: the pack reads
  * w, m, v before it, and the copy reads only the staging image.  A later
  * pack waits for the previous copy.  side_stream may equal main_stream.

@@ -769,7 +769,9 @@ int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w, const float* d_m,
     if (side != mainst)
         CUDA_TRY(cudaStreamWaitEvent(side, ctx->ev_pack, 0));
     // the header and the three regions to their file offsets in the image
-    if (ctx->copy_engine) {
+    // (the kernel writes whole 16-byte units from a 16-byte aligned image;
+    // a mapped pinned allocation starts on a page)
+    if (ctx->copy_engine || (reinterpret_cast<uintptr_t>(ctx->h_image_dev) & 15u)) {
         const size_t rb = size_t(4) * size_t(ctx->n);
         CUDA_TRY(cudaMemcpyAsync(ctx->h_image(), ctx->d_stage(0), 8, cudaMemcpyDeviceToHost,
                                  side));

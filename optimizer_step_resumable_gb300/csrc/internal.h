@@ -125,10 +125,10 @@ int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const Step
                    double clip, double grad_scale, double* partials, uint32_t* bar,
                    bool fault_test, NormResult* d_res, NormResult* h_res, int capacity,
                    bool zero_grad, void* stream);
-// Staging slots -> the pinned host image (its device address), by the SMs:
-// header (8 bytes) then w, m, v at their file offsets.
+// Staging slots -> the pinned host image (its device address), by a quarter
+// of the SMs: header (8 bytes) then w, m, v at their file offsets.
 int launch_stage_to_host(const unsigned char* header, const float* sw, const float* sm,
-                         const float* sv, int64_t n, unsigned char* image_dev, int blocks,
+                         const float* sv, int64_t n, unsigned char* image_dev, int sm_count,
                          void* stream);
 // The global result of a sharded state from the ranks' gathered sums of
 // squares (ranks.cu): published to d_res / h_res like a norm reduction.

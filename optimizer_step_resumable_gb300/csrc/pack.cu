@@ -112,69 +112,105 @@ __global__ void __launch_bounds__(kPackThreads, 4)
 // ---------------------------------------------------------------------------
 // Staging -> pinned host image, by the SMs (the side stream's alternative to
 // the copy engine).  Region r of the image starts at byte 8 + 4 n (r - 1) of
-// the page-aligned host image: 16-byte aligned when that offset is, else 8-
-// or 4-byte aligned, so each float4 read from the (256-byte aligned) slot is
-// stored as one 16-byte, two 8-byte or four 4-byte stores.  One block per SM
-// on the side stream: measured on GB300, the copy engine's copy into pinned
-// memory just written to a file took 80-116 ms for 1.33 GB where this took
-// 7-14 ms (both 6.9 ms into a fresh buffer); the concurrent steps lose about
-// 4 ms in all.
+// the page-aligned host image, which is 16-byte aligned or 4, 8 or 12 bytes
+// short of it; the kH floats up to the boundary are copied one by one, and
+// each thread then writes whole aligned 16-byte units, assembling each from
+// two neighbouring float4 of the (256-byte aligned) staging slot.
+//
+// Measured on GB300 with the 110M list (1.33 GB image): host stores stall
+// the memory pipeline of the SM that issues them, so the steps running
+// beside the copy lose time on every SM that holds a copy block.  One block
+// per SM (256 threads, 8- and 16-byte stores as the alignment allowed) cost
+// the concurrent steps 4.7 ms per checkpoint (each overlapped step 1.22 ms
+// instead of 0.436) for a 9.3 ms copy; a quarter of the SMs with 1024
+// threads each and aligned 16-byte stores copy in 7.9 ms and cost 0.39 ms.
+// The copy engine was no way out: its first copy into pages that the CPU or
+// the disk path had just touched took 50-150 ms (6.9 ms otherwise).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void copy_region_to_host(const float4* __restrict__ src,
-                                                    unsigned char* dst, int64_t n)
+constexpr int kStageThreads = 1024;
+constexpr int kStageSmsPerBlock = 4;
+
+// The 16 bytes that start kH floats into a, continuing into b.
+template <int kH>
+__device__ __forceinline__ float4 shift_floats(const float4& a, const float4& b)
 {
-    const int64_t n4 = n >> 2;
-    const int64_t gtid = int64_t(blockIdx.x) * kPackThreads + threadIdx.x;
-    const int64_t stride = int64_t(gridDim.x) * kPackThreads;
-    const unsigned mis = unsigned(reinterpret_cast<uintptr_t>(dst) & 15u);
-    if (mis == 0) {
-        float4* d = reinterpret_cast<float4*>(dst);
-        for (int64_t i = gtid; i < n4; i += stride)
-            __stcs(d + i, __ldcs(src + i));
-    } else if (mis == 8) {
-        uint2* d = reinterpret_cast<uint2*>(dst);
-        for (int64_t i = gtid; i < n4; i += stride) {
-            const float4 x = __ldcs(src + i);
-            __stcs(d + 2 * i, make_uint2(__float_as_uint(x.x), __float_as_uint(x.y)));
-            __stcs(d + 2 * i + 1, make_uint2(__float_as_uint(x.z), __float_as_uint(x.w)));
-        }
-    } else {
-        float* d = reinterpret_cast<float*>(dst);
-        for (int64_t i = gtid; i < n4; i += stride) {
-            const float4 x = __ldcs(src + i);
-            __stcs(d + 4 * i, x.x);
-            __stcs(d + 4 * i + 1, x.y);
-            __stcs(d + 4 * i + 2, x.z);
-            __stcs(d + 4 * i + 3, x.w);
-        }
-    }
-    const float* s1 = reinterpret_cast<const float*>(src);
-    float* d1 = reinterpret_cast<float*>(dst);
-    for (int64_t e = (n4 << 2) + gtid; e < n; e += stride)
-        d1[e] = s1[e];
+    if constexpr (kH == 1)
+        return make_float4(a.y, a.z, a.w, b.x);
+    else if constexpr (kH == 2)
+        return make_float4(a.z, a.w, b.x, b.y);
+    else
+        return make_float4(a.w, b.x, b.y, b.z);
 }
 
-__global__ void __launch_bounds__(kPackThreads)
+// One region: n floats from the slot src (16-byte aligned, readable up to
+// its float4 count ceil(n / 4)) to dst, whose first 16-byte boundary is kH
+// floats in.
+template <int kH>
+__device__ __forceinline__ void copy_region_to_host(const float* __restrict__ src, float* dst,
+                                                    int64_t n)
+{
+    const int64_t gtid = int64_t(blockIdx.x) * kStageThreads + threadIdx.x;
+    const int64_t stride = int64_t(gridDim.x) * kStageThreads;
+    if (kH > 0 && gtid < kH && gtid < n)
+        __stcs(dst + gtid, src[gtid]);
+    // body: dst floats [kH, kH + 4 nb) as aligned float4; the b operand of
+    // unit i is slot float4 i + 1 <= nb <= ceil(n / 4) - 1 (kH >= 1)
+    const int64_t nb = n > kH ? (n - kH) >> 2 : 0;
+    const float4* __restrict__ s4 = reinterpret_cast<const float4*>(src);
+    float4* d4 = reinterpret_cast<float4*>(dst + kH);
+    for (int64_t i = gtid; i < nb; i += stride) {
+        const float4 a = __ldcs(s4 + i);
+        if constexpr (kH == 0) {
+            __stcs(d4 + i, a);
+        } else {
+            const float4 b = __ldcs(s4 + i + 1);
+            __stcs(d4 + i, shift_floats<kH>(a, b));
+        }
+    }
+    for (int64_t e = kH + 4 * nb + gtid; e < n; e += stride)
+        __stcs(dst + e, src[e]);
+}
+
+// Floats from the start of region r (1..3) to its first 16-byte boundary,
+// for an image that starts on one: region r starts at byte 8 + 4 n (r - 1).
+template <int kNmod4, int kRegion>
+__host__ __device__ constexpr int head_floats()
+{
+    return ((16 - ((8 + 4 * kNmod4 * (kRegion - 1)) & 15)) & 15) / 4;
+}
+
+// kNmod4 = n % 4 fixes the three regions' alignment (image 16-byte aligned).
+template <int kNmod4>
+__global__ void __launch_bounds__(kStageThreads, 1)
     k_stage_to_host(const int2* __restrict__ header, const float* __restrict__ sw,
                     const float* __restrict__ sm, const float* __restrict__ sv, int64_t n,
                     unsigned char* image)
 {
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *reinterpret_cast<int2*>(image) = *header;
-    const int64_t rb = 4 * n;
-    copy_region_to_host(reinterpret_cast<const float4*>(sw), image + 8, n);
-    copy_region_to_host(reinterpret_cast<const float4*>(sm), image + 8 + rb, n);
-    copy_region_to_host(reinterpret_cast<const float4*>(sv), image + 8 + 2 * rb, n);
+    float* body = reinterpret_cast<float*>(image + 8);
+    copy_region_to_host<head_floats<kNmod4, 1>()>(sw, body, n);
+    copy_region_to_host<head_floats<kNmod4, 2>()>(sm, body + n, n);
+    copy_region_to_host<head_floats<kNmod4, 3>()>(sv, body + 2 * n, n);
 }
 
 }  // namespace
 
 int launch_stage_to_host(const unsigned char* header, const float* sw, const float* sm,
-                         const float* sv, int64_t n, unsigned char* image_dev, int blocks,
+                         const float* sv, int64_t n, unsigned char* image_dev, int sm_count,
                          void* stream)
 {
-    k_stage_to_host<<<blocks, kPackThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const int2*>(header), sw, sm, sv, n, image_dev);
+    if (reinterpret_cast<uintptr_t>(image_dev) & 15u)
+        return int(cudaErrorInvalidValue);
+    const int blocks = sm_count / kStageSmsPerBlock > 0 ? sm_count / kStageSmsPerBlock : 1;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int2* h = reinterpret_cast<const int2*>(header);
+    switch (n & 3) {
+    case 0: k_stage_to_host<0><<<blocks, kStageThreads, 0, s>>>(h, sw, sm, sv, n, image_dev); break;
+    case 1: k_stage_to_host<1><<<blocks, kStageThreads, 0, s>>>(h, sw, sm, sv, n, image_dev); break;
+    case 2: k_stage_to_host<2><<<blocks, kStageThreads, 0, s>>>(h, sw, sm, sv, n, image_dev); break;
+    default: k_stage_to_host<3><<<blocks, kStageThreads, 0, s>>>(h, sw, sm, sv, n, image_dev); break;
+    }
     return int(cudaGetLastError());
 }
 

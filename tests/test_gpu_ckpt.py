@@ -31,13 +31,15 @@ def state(dev, n, seed=7):
     return [torch.from_numpy(h).to(dev) for h in (hw, hm, hv)], (hw, hm, hv)
 
 
-@pytest.mark.parametrize("n", [1, 3, 4, 5, 6, 7, 1001, 65536, 65536 + 2, 1_000_003])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9, 1001, 65536, 65536 + 2,
+                               1_000_001, 1_000_003])
 @pytest.mark.parametrize("copy", ["kernel", "copy_engine"])
 def test_pack_write_bytes_match_oracle(dev, oracle, tmp_path, n, copy):
     """Both ways from the staging to the pinned image (the side-stream
-    kernel, whose host stores follow the regions' alignment -- 16, 8 or 4
-    bytes for n % 4 = 0, 2, odd -- and the copy engine) give the oracle's
-    bytes."""
+    kernel -- each region copied as 0-3 head floats up to a 16-byte boundary,
+    aligned 16-byte units assembled from two staging float4, a tail; n % 4
+    covers every head length, n <= 9 the cases with no or one unit -- and the
+    copy engine) give the oracle's bytes."""
     (w, m, v), hstate = state(dev, n)
     with osr.adamw_create(n) as ctx:
         osr.ckpt_set_options(ctx, 0, osr.CKPT_DIRECT | (osr.CKPT_COPY_ENGINE
