@@ -112,6 +112,23 @@ def traffic_record(kernel, workload_name):
     return None
 
 
+def copy_overlap(step_iv, copy_iv):
+    """Which timed steps ran beside each checkpoint's staging copy, and the
+    step time they lost.  step_iv: (start, end) of each step's fused kernel,
+    copy_iv: (start, end) of each copy, all in ms from one reference event.
+    A step overlaps a copy when the intervals intersect; the loss is the
+    overlapped steps' time above the median of the steps that overlap none."""
+    hit = [any(a < hi and b > lo for lo, hi in copy_iv) for a, b in step_iv]
+    clean = [b - a for (a, b), h in zip(step_iv, hit) if not h]
+    base = statistics.median(clean) if clean else None
+    out = []
+    for lo, hi in copy_iv:
+        durs = [b - a for a, b in step_iv if a < hi and b > lo]
+        out.append({"copy_ms": hi - lo, "steps_overlapped": len(durs),
+                    "step_ms_lost": (sum(durs) - len(durs) * base) if base is not None else None})
+    return out
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while running."""
 
@@ -434,6 +451,9 @@ def run_ours(args):
     norm_ms = [tr[0].elapsed_time(tr[1]) for tr in evs]
     pack_ms = [a.elapsed_time(b) for a, b, _ in pack_ev.values()]
     d2h_ms = [b.elapsed_time(c) for _, b, c in pack_ev.values()]
+    overlap = copy_overlap([(start.elapsed_time(tr[1]), start.elapsed_time(tr[2])) for tr in evs],
+                           [(start.elapsed_time(b), start.elapsed_time(c))
+                            for _, b, c in pack_ev.values()])
     norm_val, scale = osr.adamw_last_norm(ctx)
     # one synchronous checkpoint write timed on the host (outside the region)
     osr.ckpt_pack(ctx, t, w, m, v, main_stream=main, side_stream=side)
@@ -513,14 +533,22 @@ def run_ours(args):
             "d2h_ms": statistics.mean(d2h_ms), "d2h_ms_each": d2h_ms,
             "d2h_GB/s": (8 + 12 * n) / (statistics.mean(d2h_ms) / 1e3) / 1e9,
             "wait_prev_write_s_each": wait_s,
+            # the side-stream copy beside the timed steps (the last checkpoint
+            # of the region has no steps after it)
+            "copy_overlap": overlap,
             "write_fsync_s": write_s, "write_GB/s": (8 + 12 * n) / write_s / 1e9,
             "dir": "temp dir under " + (args.ckpt_dir or tempfile.gettempdir()),
             "writer": "asynchronous thread, O_DIRECT, tmp + fsync + rename",
         },
         "step_only": {"ms": statistics.mean(s + r for s, r in zip(step_ms, norm_ms)),
                       "GB/s": (STEP_BYTES + NORM_BYTES) * n /
-                      (statistics.mean(s + r for s, r in zip(step_ms, norm_ms)) / 1e3) / 1e9},
-        "gpu_launches": 2 * K + len(ck_steps),
+                      (statistics.mean(s + r for s, r in zip(step_ms, norm_ms)) / 1e3) / 1e9,
+                      "note": "norm + fused kernel per timed step; the event between them "
+                              "turns off the programmatic launch (--sweep times the step "
+                              "without it)"},
+        # per step: norm + fused (N ranks: norm, rank-order total, fused);
+        # per checkpoint: pack + staging copy
+        "gpu_launches": (2 if world == 1 else 3) * K + 2 * len(ck_steps),
         "clocks": clocks,
         "e2e": e2e,
     }

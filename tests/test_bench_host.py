@@ -1,0 +1,52 @@
+"""Host-side logic of bench.py: the copy/step overlap summary and the
+reference arm's JSON line (the CPU oracle timed on the host cores)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_copy_overlap_counts_steps_and_loss():
+    steps = [(0.0, 1.0), (1.0, 2.0), (2.0, 3.5), (3.5, 5.0), (5.0, 6.0), (6.0, 7.0)]
+    out = bench.copy_overlap(steps, [(1.5, 4.0)])
+    assert len(out) == 1
+    o = out[0]
+    assert o["copy_ms"] == pytest.approx(2.5)
+    assert o["steps_overlapped"] == 3  # (1,2), (2,3.5), (3.5,5)
+    # overlapped 1 + 1.5 + 1.5 = 4 against 3 x the median 1.0 of the others
+    assert o["step_ms_lost"] == pytest.approx(1.0)
+
+
+def test_copy_overlap_touching_intervals_do_not_overlap():
+    steps = [(0.0, 1.0), (1.0, 2.0), (2.0, 3.0)]
+    out = bench.copy_overlap(steps, [(1.0, 2.0), (3.0, 4.0)])
+    assert out[0]["steps_overlapped"] == 1 and out[0]["step_ms_lost"] == pytest.approx(0.0)
+    assert out[1]["steps_overlapped"] == 0 and out[1]["step_ms_lost"] == 0
+
+
+def test_copy_overlap_without_copies():
+    assert bench.copy_overlap([(0.0, 1.0)], []) == []
+
+
+def test_reference_arm_prints_the_contract_line():
+    r = subprocess.run(
+        [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1",
+         "--cpu-seconds", "0.25", "--workload", "flat-65536"],
+        cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["steps"] == 1 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["config"]["workload"] == "flat-65536"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
