@@ -581,6 +581,35 @@ ADAMW_API int ckpt_shard_read(adamw_ctx* ctx, const char* step_dir, int32_t rank
                               int32_t expected_world, int32_t* step_out, float* d_w,
                               float* d_m, float* d_v, void* stream);
 
+/*
+ * Resume at another world size ([S] "Three failure modes": the manifest's
+ * param_shard_offset and param_shard_numel let the loader put every shard's
+ * range back at its place in the flat parameter vector).
+ *
+ * ckpt_consolidate (host only): validates the manifest of step_dir against
+ * expected_world (< 0: any) and every shard's size and header, then writes
+ * the flat checkpoint of the whole state, <out_dir>/step_NNNNNN.bin in the
+ * ckpt_read format (n = the shards' total, which must fit an int32), by one
+ * streaming pass: the w regions of all shards in rank order, then m, then v.
+ * Each shard's sha256 is checked on the way (its bytes arrive in file
+ * order); a mismatch returns ADAMW_EFORMAT and leaves no file.  The file is
+ * made durable like ckpt_write (tmp, fsync, rename, directory fsync).
+ * path_out receives its path.
+ *
+ * ckpt_read_range: like ckpt_read, for a range of a flat checkpoint: the
+ * file may hold N >= offset + n parameters (n = the context's); copies
+ * w[offset, offset + n), m[...], v[...] to d_w, d_m, d_v and waits.  With
+ * ranges from a partition of [0, N) (for example 4-aligned equal shards) any
+ * number of ranks resumes from one consolidated file.  ADAMW_EMISMATCH if
+ * the range does not fit the file; the device arrays are untouched on
+ * failure.
+ */
+ADAMW_API int ckpt_consolidate(const char* step_dir, int32_t expected_world,
+                               const char* out_dir, char* path_out, size_t path_cap);
+ADAMW_API int ckpt_read_range(adamw_ctx* ctx, const char* path, int64_t offset,
+                              int32_t* step_out, float* d_w, float* d_m, float* d_v,
+                              void* stream);
+
 /* SHA-256 (FIPS 180-4) of `bytes` bytes as 64 lowercase hex digits + NUL. */
 ADAMW_API int ckpt_sha256_hex(const void* data, int64_t bytes, char* hex_out);
 

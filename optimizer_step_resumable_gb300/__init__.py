@@ -98,6 +98,10 @@ SIGNATURES = {
                                       _c.c_int32]),
     "ckpt_shard_read": (_c.c_int, [_vp, _c.c_char_p, _c.c_int32, _c.c_int32,
                                    _c.POINTER(_c.c_int32), _vp, _vp, _vp, _vp]),
+    "ckpt_consolidate": (_c.c_int, [_c.c_char_p, _c.c_int32, _c.c_char_p, _c.c_char_p,
+                                    _c.c_size_t]),
+    "ckpt_read_range": (_c.c_int, [_vp, _c.c_char_p, _c.c_int64, _c.POINTER(_c.c_int32), _vp,
+                                   _vp, _vp, _vp]),
     "ckpt_sha256_hex": (_c.c_int, [_vp, _c.c_int64, _c.c_char_p]),
     "adamw_strerror": (_c.c_char_p, [_c.c_int]),
     "adamw_last_error": (_c.c_char_p, []),
@@ -614,6 +618,28 @@ def ckpt_shard_read(ctx: Context, step_dir: str, rank: int, w, m, v, expected_wo
                                    int(expected_world), ctypes.byref(step), _dev_ptr(w, n, "w"),
                                    _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), _stream(stream))
     _check(st, "ckpt_shard_read")
+    return step.value
+
+
+def ckpt_consolidate(step_dir: str, out_dir: str, expected_world: int = -1) -> str:
+    """Writes the flat checkpoint of a sharded one (every shard's sha256
+    checked on the way) as <out_dir>/step_NNNNNN.bin; returns its path."""
+    buf = ctypes.create_string_buffer(4200)
+    st = library().ckpt_consolidate(os.fsencode(step_dir), int(expected_world),
+                                    os.fsencode(out_dir), buf, len(buf))
+    _check(st, "ckpt_consolidate")
+    return buf.value.decode()
+
+
+def ckpt_read_range(ctx: Context, path: str, offset: int, w, m, v, stream=None) -> int:
+    """Reads parameters [offset, offset + ctx.n) of a flat checkpoint into
+    w, m, v; returns the stored step."""
+    n = ctx.n
+    step = ctypes.c_int32(-1)
+    st = library().ckpt_read_range(ctx.handle, os.fsencode(path), int(offset),
+                                   ctypes.byref(step), _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"),
+                                   _dev_ptr(v, n, "v"), _stream(stream))
+    _check(st, "ckpt_read_range")
     return step.value
 
 

@@ -834,4 +834,53 @@ int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out, float* d_w, f
     return ADAMW_OK;
 }
 
+int ckpt_read_range(adamw_ctx* ctx, const char* path, int64_t offset, int32_t* step_out,
+                    float* d_w, float* d_m, float* d_v, void* stream)
+{
+    osr::clear_error();
+    if (!ctx || !path)
+        return fail(ADAMW_EINVAL, "ctx or path is NULL");
+    if (!ctx->has_ckpt)
+        return fail(ADAMW_ESTATE, "context was created without checkpoint staging");
+    int rc;
+    if ((rc = check_state_ptr(d_w, "d_w")) || (rc = check_state_ptr(d_m, "d_m")) ||
+        (rc = check_state_ptr(d_v, "d_v")))
+        return rc;
+    if (offset < 0)
+        return fail(ADAMW_EINVAL, "offset=%lld is negative", (long long)offset);
+    osr::writer_drain(ctx);
+    DeviceScope scope(ctx->device);
+    if (ctx->d2h_pending) {
+        CUDA_TRY(cudaEventSynchronize(ctx->ev_d2h));
+        ctx->d2h_pending = false;
+    }
+    int32_t step = -1, nf = -1;
+    int fd = -1;
+    rc = osr::open_validated(path, -1, &step, &nf, &fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    if (offset + ctx->n > int64_t(nf)) {
+        ::close(fd);
+        return fail(ADAMW_EMISMATCH, "%s holds %d parameters; [%lld, %lld) is out of range", path,
+                    nf, (long long)offset, (long long)(offset + ctx->n));
+    }
+    ctx->packed = false;  // the pinned image is about to hold the file's range
+    const size_t bytes = size_t(ctx->n) * 4u;
+    unsigned char* body = ctx->h_image() + 8;
+    for (int r = 0; r < 3 && rc == ADAMW_OK; ++r)
+        rc = osr::pread_exact(fd, body + size_t(r) * bytes, bytes,
+                              8 + 4 * (int64_t(nf) * r + offset), path);
+    ::close(fd);
+    if (rc != ADAMW_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaMemcpyAsync(d_w, body, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(d_m, body + bytes, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(d_v, body + 2 * bytes, bytes, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (step_out)
+        *step_out = step;
+    return ADAMW_OK;
+}
+
 }  // extern "C"

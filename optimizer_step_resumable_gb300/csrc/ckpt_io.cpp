@@ -239,6 +239,87 @@ int rotate_files(const char* dir, int32_t keep, int32_t* removed)
     return rc;
 }
 
+int pread_exact(int fd, void* dst, size_t bytes, int64_t offset, const char* path)
+{
+    unsigned char* p = static_cast<unsigned char*>(dst);
+    while (bytes > 0) {
+        const size_t want = bytes > (size_t(1) << 30) ? (size_t(1) << 30) : bytes;
+        const ssize_t got = ::pread(fd, p, want, off_t(offset));
+        if (got < 0) {
+            if (errno == EINTR)
+                continue;
+            return fail(ADAMW_EIO, "read %s: %s", path, std::strerror(errno));
+        }
+        if (got == 0)
+            return fail(ADAMW_ESIZE, "%s: file ended early", path);
+        p += got;
+        offset += got;
+        bytes -= size_t(got);
+    }
+    return ADAMW_OK;
+}
+
+AtomicFile::~AtomicFile()
+{
+    if (fd_ >= 0) {
+        ::close(fd_);
+        ::unlink(tmp_.c_str());
+    }
+}
+
+int AtomicFile::open(const char* dir, const char* name)
+{
+    if (!dir || !name)
+        return fail(ADAMW_EINVAL, "ckpt write: null directory or name");
+    if (fd_ >= 0)
+        return fail(ADAMW_ESTATE, "ckpt write: file already open");
+    dir_ = dir;
+    final_ = dir_ + "/" + name;
+    tmp_ = final_ + ".tmp";
+    if (final_.size() >= 4096)
+        return fail(ADAMW_EINVAL, "ckpt write: directory name too long");
+    fd_ = ::open(tmp_.c_str(), O_WRONLY | O_CREAT | O_TRUNC | O_CLOEXEC, 0644);
+    if (fd_ < 0)
+        return fail(ADAMW_EIO, "open %s: %s", tmp_.c_str(), std::strerror(errno));
+    return ADAMW_OK;
+}
+
+int AtomicFile::write(const void* data, size_t bytes)
+{
+    if (fd_ < 0)
+        return fail(ADAMW_ESTATE, "ckpt write: no open file");
+    return write_exact(fd_, data, bytes, tmp_.c_str());
+}
+
+int AtomicFile::commit(char* path_out, size_t path_cap)
+{
+    if (fd_ < 0)
+        return fail(ADAMW_ESTATE, "ckpt write: no open file");
+    int rc = ADAMW_OK;
+    if (::fsync(fd_) != 0)
+        rc = fail(ADAMW_EIO, "fsync %s: %s", tmp_.c_str(), std::strerror(errno));
+    if (::close(fd_) != 0 && rc == ADAMW_OK)
+        rc = fail(ADAMW_EIO, "close %s: %s", tmp_.c_str(), std::strerror(errno));
+    fd_ = -1;
+    if (rc == ADAMW_OK && ::rename(tmp_.c_str(), final_.c_str()) != 0)
+        rc = fail(ADAMW_EIO, "rename %s: %s", tmp_.c_str(), std::strerror(errno));
+    if (rc != ADAMW_OK) {
+        ::unlink(tmp_.c_str());
+        return rc;
+    }
+    const int dfd = ::open(dir_.c_str(), O_RDONLY | O_CLOEXEC);
+    if (dfd >= 0) {
+        ::fsync(dfd);
+        ::close(dfd);
+    }
+    if (path_out && path_cap > 0) {
+        if (final_.size() + 1 > path_cap)
+            return fail(ADAMW_EINVAL, "ckpt write: path buffer too small (file written)");
+        std::memcpy(path_out, final_.c_str(), final_.size() + 1);
+    }
+    return ADAMW_OK;
+}
+
 int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
                    int32_t* n_out, int* fd_out)
 {

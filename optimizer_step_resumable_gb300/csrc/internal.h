@@ -249,5 +249,24 @@ int load_manifest(const char* step_dir, int32_t expected_world, bool verify, int
 int open_validated(const char* path, int32_t n_expected, int32_t* step_out,
                    int32_t* n_out, int* fd_out);
 int read_exact(int fd, void* dst, size_t bytes, const char* path);
+// Reads exactly bytes at offset; ADAMW_ESIZE if the file ends first.
+int pread_exact(int fd, void* dst, size_t bytes, int64_t offset, const char* path);
+// A file written in pieces and made visible atomically: <dir>/<name>.tmp,
+// then commit() fsyncs it, renames it over <dir>/<name> and fsyncs dir.
+// Destroyed without a commit, it removes the .tmp.
+class AtomicFile {
+public:
+    AtomicFile() = default;
+    AtomicFile(const AtomicFile&) = delete;
+    AtomicFile& operator=(const AtomicFile&) = delete;
+    ~AtomicFile();
+    int open(const char* dir, const char* name);
+    int write(const void* data, size_t bytes);
+    int commit(char* path_out, size_t path_cap);
+
+private:
+    int fd_ = -1;
+    std::string dir_, tmp_, final_;
+};
 
 }  // namespace osr

@@ -597,4 +597,100 @@ int ckpt_manifest_load(const char* step_dir, int32_t expected_world, int32_t ver
     return ADAMW_OK;
 }
 
+// The flat state from the shards (section "Three failure modes the schema
+// must guard against": each shard's param_shard_offset and param_shard_numel
+// put its range back at its place in the flat parameter vector).  Streams
+// the w regions of all shards in rank order, then the m regions, then the v
+// regions, into <out_dir>/step_NNNNNN.bin (atomic: .tmp, fsync, rename).  A
+// shard's bytes reach its SHA-256 in file order (header, w, m, v), so every
+// digest is checked without a second read; on a mismatch no file appears.
+int ckpt_consolidate(const char* step_dir, int32_t expected_world, const char* out_dir,
+                     char* path_out, size_t path_cap)
+{
+    osr::clear_error();
+    if (!step_dir || !out_dir)
+        return osr::fail(ADAMW_EINVAL, "ckpt_consolidate: null directory");
+    std::vector<int64_t> off, num;
+    std::vector<std::string> paths, digests;
+    int32_t step = -1;
+    int rc = osr::load_manifest(step_dir, expected_world, false, &step, &off, &num, &paths,
+                                &digests);
+    if (rc != ADAMW_OK)
+        return rc;
+    const size_t world = off.size();
+    const int64_t n = off.back() + num.back();
+    if (n > INT32_MAX)
+        return osr::fail(ADAMW_ESIZE, "%s: %lld parameters in all do not fit the header",
+                         step_dir, (long long)n);
+    auto le_header = [](int32_t a, int32_t b, unsigned char* h) {
+        for (int i = 0; i < 4; ++i) {
+            h[i] = static_cast<unsigned char>((uint32_t(a) >> (8 * i)) & 0xffu);
+            h[4 + i] = static_cast<unsigned char>((uint32_t(b) >> (8 * i)) & 0xffu);
+        }
+    };
+    std::vector<int> fds(world, -1);
+    std::vector<osr::Sha256> hashes(world);
+    std::vector<std::string> spaths(world);
+    auto close_all = [&] {
+        for (int& fd : fds)
+            if (fd >= 0) {
+                ::close(fd);
+                fd = -1;
+            }
+    };
+    for (size_t r = 0; r < world && rc == ADAMW_OK; ++r) {
+        spaths[r] = std::string(step_dir) + "/" + paths[r];
+        int32_t fstep = -1, fn = -1;
+        rc = osr::open_validated(spaths[r].c_str(), int32_t(num[r]), &fstep, &fn, &fds[r]);
+        if (rc == ADAMW_OK && fstep != step)
+            rc = osr::fail(ADAMW_EMISMATCH, "%s: step %d, manifest says %d", spaths[r].c_str(),
+                           fstep, step);
+        if (rc == ADAMW_OK) {
+            unsigned char h[8];
+            le_header(fstep, fn, h);
+            hashes[r].update(h, 8);
+        }
+    }
+    if (rc != ADAMW_OK) {
+        close_all();
+        return rc;
+    }
+    char name[32];
+    std::snprintf(name, sizeof name, "step_%06d.bin", int(step));
+    osr::AtomicFile out;
+    rc = out.open(out_dir, name);
+    if (rc == ADAMW_OK) {
+        unsigned char h[8];
+        le_header(step, int32_t(n), h);
+        rc = out.write(h, 8);
+    }
+    std::vector<unsigned char> buf(size_t(8) << 20);
+    for (int region = 0; region < 3 && rc == ADAMW_OK; ++region)
+        for (size_t r = 0; r < world && rc == ADAMW_OK; ++r) {
+            int64_t pos = 8 + 4 * num[r] * region;
+            int64_t left = 4 * num[r];
+            while (left > 0 && rc == ADAMW_OK) {
+                const size_t k = left < int64_t(buf.size()) ? size_t(left) : buf.size();
+                rc = osr::pread_exact(fds[r], buf.data(), k, pos, spaths[r].c_str());
+                if (rc == ADAMW_OK) {
+                    hashes[r].update(buf.data(), k);
+                    rc = out.write(buf.data(), k);
+                }
+                pos += int64_t(k);
+                left -= int64_t(k);
+            }
+        }
+    close_all();
+    for (size_t r = 0; r < world && rc == ADAMW_OK; ++r) {
+        char hex[65];
+        hashes[r].final_hex(hex);
+        if (digests[r] != hex)
+            rc = osr::fail(ADAMW_EFORMAT, "%s: sha256 %s, manifest says %s (partial or corrupted "
+                           "write)", spaths[r].c_str(), hex, digests[r].c_str());
+    }
+    if (rc != ADAMW_OK)
+        return rc;  // the unfinished .tmp goes with `out`
+    return out.commit(path_out, path_cap);
+}
+
 }  // extern "C"

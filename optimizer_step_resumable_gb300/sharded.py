@@ -13,8 +13,9 @@ from __future__ import annotations
 
 import time
 
-from . import (adamw_clip_step_ex, adamw_clip_step_gathered, ckpt_manifest_commit, ckpt_pack,
-               ckpt_shard_read, ckpt_shard_write, grad_sumsq, grad_sumsq_to)
+from . import (adamw_clip_step_ex, adamw_clip_step_gathered, ckpt_consolidate,
+               ckpt_manifest_commit, ckpt_pack, ckpt_probe, ckpt_read_range, ckpt_shard_read,
+               ckpt_shard_write, grad_sumsq, grad_sumsq_to)
 
 
 def shard_range(n: int, rank: int, world: int, align: int = 4):
@@ -125,3 +126,20 @@ def load_sharded(ctx, step_dir, rank, world, w, m, v, stream=None):
     """Reads this rank's shard after validating the manifest against the
     world size and the shard's sha256; returns the stored step."""
     return ckpt_shard_read(ctx, step_dir, rank, w, m, v, expected_world=world, stream=stream)
+
+
+def consolidate(step_dir, out_dir, expected_world=-1):
+    """The flat step_NNNNNN.bin of a sharded checkpoint (host only; every
+    shard's sha256 checked); returns its path."""
+    return ckpt_consolidate(step_dir, out_dir, expected_world)
+
+
+def load_range(ctx, flat_path, rank, world, w, m, v, stream=None):
+    """This rank's shard_range of a flat checkpoint -- for example one
+    consolidated from a run with another world size -- into w, m, v (the
+    context holds exactly that range); returns the stored step."""
+    _, n_total = ckpt_probe(flat_path)
+    off, numel = shard_range(n_total, rank, world)
+    if numel != ctx.n:
+        raise ValueError(f"rank {rank} of {world} owns {numel} parameters, the context {ctx.n}")
+    return ckpt_read_range(ctx, flat_path, off, w, m, v, stream=stream)

@@ -184,3 +184,82 @@ def test_gloo_ranks_write_one_checkpoint(lib, tmp_path, world):
     for r, (_, _, w, m, v) in enumerate(got):
         ref = np.load(tmp_path / f"in{r}.npy")
         assert w.tobytes() == ref[0].tobytes() and v.tobytes() == ref[2].tobytes()
+
+
+# ---------------------------------------------------------------------------
+# Consolidation: the shards' ranges put back at their offsets of the flat
+# vector, as one step_NNNNNN.bin.
+# ---------------------------------------------------------------------------
+def _flat(n, seed=11):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal(n).astype(np.float32) for _ in range(3)]
+
+
+def _split(flat, world):
+    from optimizer_step_resumable_gb300 import sharded
+    n = flat[0].size
+    ranges = [sharded.shard_range(n, r, world) for r in range(world)]
+    return ranges, [tuple(a[o:o + k] for a in flat) for o, k in ranges]
+
+
+def _flat_bytes(step, flat):
+    import struct
+    return struct.pack("<ii", step, flat[0].size) + b"".join(a.tobytes() for a in flat)
+
+
+@pytest.mark.parametrize("n,world", [(3997, 4), (4096, 1), (10, 3), (7, 7), (65_537, 5)])
+def test_consolidate_puts_shards_at_their_offsets(lib, oracle, tmp_path, n, world):
+    flat = _flat(n)
+    ranges, shards = _split(flat, world)
+    digests = [osr.ckpt_shard_write_host(str(tmp_path), 300, r, *s) for r, s in enumerate(shards)]
+    d = osr.ckpt_manifest_commit(str(tmp_path), 300, [o for o, _ in ranges],
+                                 [k for _, k in ranges], digests, 1.0)
+    out = tmp_path / "flat"
+    out.mkdir()
+    path = osr.ckpt_consolidate(d, str(out), expected_world=world)
+    assert path == str(out / "step_000300.bin")
+    assert sorted(os.listdir(out)) == ["step_000300.bin"]  # no .tmp left
+    assert open(path, "rb").read() == _flat_bytes(300, flat)
+    st, step, ow, om, ov = oracle.ckpt_read(path, n)  # the oracle's reader agrees
+    assert st == 0 and step == 300
+    assert ow.tobytes() == flat[0].tobytes() and ov.tobytes() == flat[2].tobytes()
+    assert osr.ckpt_probe(path) == (300, n)
+
+
+def test_consolidate_of_oracle_written_shards(lib, tmp_path):
+    sizes = [1000, 24, 3]
+    shards = _shards(sizes, 5)
+    d = osh.save_sharded(str(tmp_path), 7, shards, _offsets(sizes), 2.0)
+    path = osr.ckpt_consolidate(d, str(tmp_path))
+    flat = [np.concatenate([s[i] for s in shards]) for i in range(3)]
+    assert open(path, "rb").read() == _flat_bytes(7, flat)
+
+
+def test_consolidate_refuses_and_leaves_no_file(lib, tmp_path):
+    flat = _flat(2000)
+    ranges, shards = _split(flat, 4)
+    src = tmp_path / "src"
+    src.mkdir()
+    digests = [osr.ckpt_shard_write_host(str(src), 12, r, *s) for r, s in enumerate(shards)]
+    d = osr.ckpt_manifest_commit(str(src), 12, [o for o, _ in ranges], [k for _, k in ranges],
+                                 digests, 0.0)
+    out = tmp_path / "out"
+    out.mkdir()
+    with pytest.raises(osr.AdamWError) as e:  # a different world size
+        osr.ckpt_consolidate(d, str(out), expected_world=3)
+    assert e.value.status == osr.EMISMATCH
+    # one flipped bit in the last shard's v region: found by the digest only
+    # after every other byte was streamed; the output never appears
+    p = os.path.join(d, "rank3.bin")
+    data = bytearray(open(p, "rb").read())
+    data[-5] ^= 0x01
+    open(p, "wb").write(bytes(data))
+    with pytest.raises(osr.AdamWError) as e:
+        osr.ckpt_consolidate(d, str(out), expected_world=4)
+    assert e.value.status == osr.EFORMAT
+    assert os.listdir(out) == []
+    open(p, "wb").write(bytes(data[:-4]))  # truncated: refused before writing
+    with pytest.raises(osr.AdamWError) as e:
+        osr.ckpt_consolidate(d, str(out))
+    assert e.value.status == osr.ESIZE
+    assert os.listdir(out) == []
