@@ -165,7 +165,12 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dev_ptr(t, n: int, name: str) -> int:
+def _same_device(t, name: str, ctx) -> None:
+    if ctx is not None and ctx.device is not None and t.device.index != ctx.device:
+        raise ValueError(f"{name} is on cuda:{t.device.index}, the context on cuda:{ctx.device}")
+
+
+def _dev_ptr(t, n: int, name: str, ctx=None) -> int:
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -173,15 +178,17 @@ def _dev_ptr(t, n: int, name: str) -> int:
         raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
     if t.numel() != n:
         raise ValueError(f"{name} has {t.numel()} elements, context has {n}")
+    _same_device(t, name, ctx)
     return t.data_ptr()
 
 
 class Context:
     """Owner of one ``adamw_ctx*``; freed by ``adamw_destroy`` or on GC."""
 
-    def __init__(self, handle: int, n: int):
+    def __init__(self, handle: int, n: int, device=None):
         self.handle = handle
         self.n = n
+        self.device = device  # CUDA device index the context was created on
 
     @property
     def num_tensors(self) -> int:
@@ -221,7 +228,8 @@ def adamw_create(n_params: int, offsets=None, numels=None, flags: int = 0) -> Co
                           pn and ctypes.addressof(pn), nt, int(flags), ctypes.byref(out))
     del keep
     _check(st, "adamw_create")
-    return Context(out.value, int(n_params))
+    import torch
+    return Context(out.value, int(n_params), torch.cuda.current_device())
 
 
 def adamw_destroy(ctx: Context):
@@ -235,7 +243,7 @@ def adamw_set_hparams(ctx: Context, beta1: float, beta2: float, eps: float):
 def grad_global_norm(ctx: Context, g, wait: bool = True, stream=None):
     """||g||_2; with wait=False returns None and leaves it in the context."""
     out = ctypes.c_double()
-    st = library().grad_global_norm(ctx.handle, _dev_ptr(g, ctx.n, "g"),
+    st = library().grad_global_norm(ctx.handle, _dev_ptr(g, ctx.n, "g", ctx),
                                     ctypes.byref(out) if wait else None, _stream(stream))
     _check(st, "grad_global_norm")
     return out.value if wait else None
@@ -244,8 +252,8 @@ def grad_global_norm(ctx: Context, g, wait: bool = True, stream=None):
 def adamw_clip_step(ctx: Context, w, g, m, v, t: int, lr: float, wd: float,
                     clip: float, stream=None):
     n = ctx.n
-    st = library().adamw_clip_step(ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"),
-                                   _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), int(t),
+    st = library().adamw_clip_step(ctx.handle, _dev_ptr(w, n, "w", ctx), _dev_ptr(g, n, "g", ctx),
+                                   _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx), int(t),
                                    float(lr), float(wd), float(clip), _stream(stream))
     _check(st, "adamw_clip_step")
 
@@ -259,8 +267,8 @@ def adamw_clip_step_ex(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, c
     n = ctx.n
     flags = (ZERO_GRAD if zero_grad else 0) | (TENSOR_NORMS if tensor_norms else 0)
     st = library().adamw_clip_step_ex(
-        ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"), _dev_ptr(m, n, "m"),
-        _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip), float(grad_scale),
+        ctx.handle, _dev_ptr(w, n, "w", ctx), _dev_ptr(g, n, "g", ctx), _dev_ptr(m, n, "m", ctx),
+        _dev_ptr(v, n, "v", ctx), int(t), float(lr), float(wd), float(clip), float(grad_scale),
         float(global_sumsq), flags, _stream(stream))
     _check(st, "adamw_clip_step_ex")
 
@@ -273,12 +281,13 @@ def _dtype_of(t):
     return table[t.dtype]
 
 
-def _typed_ptr(t, n: int, name: str) -> int:
+def _typed_ptr(t, n: int, name: str, ctx=None) -> int:
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
         raise TypeError(f"{name} must be a contiguous CUDA tensor")
     if t.numel() != n:
         raise ValueError(f"{name} has {t.numel()} elements, context has {n}")
+    _same_device(t, name, ctx)
     return t.data_ptr()
 
 
@@ -291,37 +300,38 @@ def adamw_clip_step_mixed(ctx: Context, w, g, m, v, t: int, lr: float, wd: float
     flags = (ZERO_GRAD if zero_grad else 0) | (TENSOR_NORMS if tensor_norms else 0)
     lp_ptr, lp_dt = None, DTYPE_BF16
     if w_lp is not None:
-        lp_ptr, lp_dt = _typed_ptr(w_lp, n, "w_lp"), _dtype_of(w_lp)
+        lp_ptr, lp_dt = _typed_ptr(w_lp, n, "w_lp", ctx), _dtype_of(w_lp)
         if lp_dt == DTYPE_F32:
             raise TypeError("w_lp must be bfloat16 or float16")
     st = library().adamw_clip_step_mixed(
-        ctx.handle, _dev_ptr(w, n, "w"), _typed_ptr(g, n, "g"), _dtype_of(g), _dev_ptr(m, n, "m"),
-        _dev_ptr(v, n, "v"), lp_ptr, lp_dt, int(t), float(lr), float(wd), float(clip),
+        ctx.handle, _dev_ptr(w, n, "w", ctx), _typed_ptr(g, n, "g", ctx), _dtype_of(g), _dev_ptr(m, n, "m", ctx),
+        _dev_ptr(v, n, "v", ctx), lp_ptr, lp_dt, int(t), float(lr), float(wd), float(clip),
         float(grad_scale), float(global_sumsq), flags, _stream(stream))
     _check(st, "adamw_clip_step_mixed")
 
 
 def grad_sumsq_typed(ctx: Context, g, stream=None) -> float:
     out = ctypes.c_double()
-    st = library().grad_sumsq_typed(ctx.handle, _typed_ptr(g, ctx.n, "g"), _dtype_of(g),
+    st = library().grad_sumsq_typed(ctx.handle, _typed_ptr(g, ctx.n, "g", ctx), _dtype_of(g),
                                     ctypes.byref(out), _stream(stream))
     _check(st, "grad_sumsq_typed")
     return out.value
 
 
-def _f64_dev_ptr(t, k: int, name: str) -> int:
+def _f64_dev_ptr(t, k: int, name: str, ctx=None) -> int:
     import torch
     if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float64
             and t.is_contiguous() and t.numel() >= k):
         raise ValueError(f"{name} must be a contiguous CUDA float64 tensor of >= {k} values")
+    _same_device(t, name, ctx)
     return t.data_ptr()
 
 
 def grad_sumsq_to(ctx: Context, g, out, stream=None):
     """This shard's sum of g^2 written to the CUDA float64 tensor `out`
     (its first element) on the stream, with no host wait."""
-    st = library().grad_sumsq_to(ctx.handle, _typed_ptr(g, ctx.n, "g"), _dtype_of(g),
-                                 _f64_dev_ptr(out, 1, "out"), _stream(stream))
+    st = library().grad_sumsq_to(ctx.handle, _typed_ptr(g, ctx.n, "g", ctx), _dtype_of(g),
+                                 _f64_dev_ptr(out, 1, "out", ctx), _stream(stream))
     _check(st, "grad_sumsq_to")
 
 
@@ -334,9 +344,9 @@ def adamw_clip_step_gathered(ctx: Context, w, g, m, v, t: int, lr: float, wd: fl
     n = ctx.n
     world = rank_sumsq.numel()
     st = library().adamw_clip_step_gathered(
-        ctx.handle, _dev_ptr(w, n, "w"), _typed_ptr(g, n, "g"), _dtype_of(g),
-        _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), int(t), float(lr), float(wd), float(clip),
-        float(grad_scale), _f64_dev_ptr(rank_sumsq, world, "rank_sumsq"), int(world),
+        ctx.handle, _dev_ptr(w, n, "w", ctx), _typed_ptr(g, n, "g", ctx), _dtype_of(g),
+        _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx), int(t), float(lr), float(wd), float(clip),
+        float(grad_scale), _f64_dev_ptr(rank_sumsq, world, "rank_sumsq", ctx), int(world),
         ZERO_GRAD if zero_grad else 0, _stream(stream))
     _check(st, "adamw_clip_step_gathered")
 
@@ -346,7 +356,7 @@ def grad_tensor_sumsq(ctx: Context, g, stream=None):
     NonFiniteGradient (with .values set) if the global sum is not finite."""
     import numpy as np
     out = np.empty(ctx.num_tensors, np.float64)
-    st = library().grad_tensor_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g"), out.ctypes.data,
+    st = library().grad_tensor_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g", ctx), out.ctypes.data,
                                      _stream(stream))
     if st == ENONFINITE:
         err = NonFiniteGradient(st, "grad_tensor_sumsq", adamw_last_error())
@@ -367,7 +377,7 @@ def adamw_last_tensor_sumsq(ctx: Context):
 def grad_sumsq(ctx: Context, g, stream=None) -> float:
     """Sum of g^2 over the context's n values (waits); raises NonFiniteGradient."""
     out = ctypes.c_double()
-    st = library().grad_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g"), ctypes.byref(out),
+    st = library().grad_sumsq(ctx.handle, _dev_ptr(g, ctx.n, "g", ctx), ctypes.byref(out),
                               _stream(stream))
     _check(st, "grad_sumsq")
     return out.value
@@ -375,8 +385,8 @@ def grad_sumsq(ctx: Context, g, stream=None) -> float:
 
 def adamw_graph_create(ctx: Context, w, g, m, v):
     n = ctx.n
-    _check(library().adamw_graph_create(ctx.handle, _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"),
-                                        _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v")),
+    _check(library().adamw_graph_create(ctx.handle, _dev_ptr(w, n, "w", ctx), _dev_ptr(g, n, "g", ctx),
+                                        _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx)),
            "adamw_graph_create")
 
 
@@ -403,15 +413,17 @@ def adamw_clip_step_noalloc(w, g, m, v, t: int, lr: float, wd: float, clip: floa
     """The clipped-AdamW step without a context, for callers that must not
     allocate GPU memory (see include/adamw_ckpt.h).  norm_out: optional
     float64 CUDA tensor of one element that receives the gradient norm."""
+    import types
+
     import torch
     n = w.numel()
+    here = types.SimpleNamespace(device=torch.cuda.current_device())  # the launch device
     np_ = None
     if norm_out is not None:
-        if not (norm_out.is_cuda and norm_out.dtype == torch.float64 and norm_out.numel() >= 1):
-            raise TypeError("norm_out must be a float64 CUDA tensor")
-        np_ = norm_out.data_ptr()
+        np_ = _f64_dev_ptr(norm_out, 1, "norm_out", here)
     st = library().adamw_clip_step_noalloc(
-        _dev_ptr(w, n, "w"), _dev_ptr(g, n, "g"), _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"),
+        _dev_ptr(w, n, "w", here), _dev_ptr(g, n, "g", here), _dev_ptr(m, n, "m", here),
+        _dev_ptr(v, n, "v", here),
         int(n), int(t), float(lr), float(wd), float(clip), float(beta1), float(beta2),
         float(eps), np_, _stream(stream))
     _check(st, "adamw_clip_step_noalloc")
@@ -445,8 +457,8 @@ def ckpt_pack(ctx: Context, step: int, w, m, v, main_stream=None, side_stream=No
     n = ctx.n
     ms = _stream(main_stream)
     ss = ms if side_stream is None else _stream(side_stream)
-    st = library().ckpt_pack(ctx.handle, int(step), _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"),
-                             _dev_ptr(v, n, "v"), ms, ss)
+    st = library().ckpt_pack(ctx.handle, int(step), _dev_ptr(w, n, "w", ctx), _dev_ptr(m, n, "m", ctx),
+                             _dev_ptr(v, n, "v", ctx), ms, ss)
     _check(st, "ckpt_pack")
 
 
@@ -479,8 +491,8 @@ def ckpt_step_end(ctx: Context, step: int, w, m, v, directory: str, every: int,
     ms = _stream(main_stream)
     ss = ms if side_stream is None else _stream(side_stream)
     action = ctypes.c_int32(0)
-    st = library().ckpt_step_end(ctx.handle, int(step), _dev_ptr(w, n, "w"),
-                                 _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), ms, ss,
+    st = library().ckpt_step_end(ctx.handle, int(step), _dev_ptr(w, n, "w", ctx),
+                                 _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx), ms, ss,
                                  os.fsencode(directory), int(every), ctypes.byref(action))
     _check(st, "ckpt_step_end")
     return action.value
@@ -519,7 +531,7 @@ def ckpt_read(ctx: Context, path: str, w, m, v, stream=None) -> int:
     n = ctx.n
     step = ctypes.c_int32(-1)
     st = library().ckpt_read(ctx.handle, os.fsencode(path), ctypes.byref(step),
-                             _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"),
+                             _dev_ptr(w, n, "w", ctx), _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx),
                              _stream(stream))
     _check(st, "ckpt_read")
     return step.value
@@ -615,8 +627,8 @@ def ckpt_shard_read(ctx: Context, step_dir: str, rank: int, w, m, v, expected_wo
     n = ctx.n
     step = ctypes.c_int32(-1)
     st = library().ckpt_shard_read(ctx.handle, os.fsencode(step_dir), int(rank),
-                                   int(expected_world), ctypes.byref(step), _dev_ptr(w, n, "w"),
-                                   _dev_ptr(m, n, "m"), _dev_ptr(v, n, "v"), _stream(stream))
+                                   int(expected_world), ctypes.byref(step), _dev_ptr(w, n, "w", ctx),
+                                   _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx), _stream(stream))
     _check(st, "ckpt_shard_read")
     return step.value
 
@@ -637,8 +649,8 @@ def ckpt_read_range(ctx: Context, path: str, offset: int, w, m, v, stream=None) 
     n = ctx.n
     step = ctypes.c_int32(-1)
     st = library().ckpt_read_range(ctx.handle, os.fsencode(path), int(offset),
-                                   ctypes.byref(step), _dev_ptr(w, n, "w"), _dev_ptr(m, n, "m"),
-                                   _dev_ptr(v, n, "v"), _stream(stream))
+                                   ctypes.byref(step), _dev_ptr(w, n, "w", ctx), _dev_ptr(m, n, "m", ctx),
+                                   _dev_ptr(v, n, "v", ctx), _stream(stream))
     _check(st, "ckpt_read_range")
     return step.value
 

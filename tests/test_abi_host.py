@@ -169,3 +169,15 @@ def test_killed_writer_leaves_a_complete_file(lib, oracle, tmp_path):
         final = d / "step_000100.bin"
         assert osr.ckpt_probe(str(final), n) == (100, n)
         assert final.read_bytes() in images
+
+
+def test_binding_refuses_tensors_of_another_device():
+    """Pointers handed to a context must live on its device (a tensor of
+    another GPU would give the kernels an address of the wrong memory)."""
+    import types
+    ctx = types.SimpleNamespace(device=0)
+    on = lambda i: types.SimpleNamespace(device=types.SimpleNamespace(index=i))  # noqa: E731
+    osr._same_device(on(0), "w", ctx)
+    osr._same_device(on(1), "w", None)  # no context: nothing to compare
+    with pytest.raises(ValueError, match="cuda:1, the context on cuda:0"):
+        osr._same_device(on(1), "w", ctx)
