@@ -37,7 +37,7 @@ def nvcc() -> str:
 
 def _sources():
     return ([os.path.join(CSRC, s) for s in CUDA_SOURCES + CXX_SOURCES]
-            + [os.path.join(CSRC, h) for h in ("internal.h", "common.cuh", "context.h",
+            + [os.path.join(CSRC, h) for h in ("internal.h", "ckpt_io.h", "common.cuh", "context.h",
                                                  "norm_dev.cuh", "adamw_dev.cuh")]
             + [os.path.join(INCLUDE, "adamw_ckpt.h")])
 

@@ -10,6 +10,7 @@
 
 #include <cuda_runtime.h>
 
+#include "ckpt_io.h"
 #include "internal.h"
 
 namespace osr {

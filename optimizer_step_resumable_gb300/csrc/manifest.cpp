@@ -30,6 +30,7 @@
 #include <sys/stat.h>
 #include <unistd.h>
 
+#include "ckpt_io.h"
 #include "internal.h"
 
 namespace osr {

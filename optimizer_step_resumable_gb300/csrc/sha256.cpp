@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "ckpt_io.h"
 #include "internal.h"
 
 namespace osr {
