@@ -259,7 +259,8 @@ ADAMW_API int adamw_clip_step_gathered(adamw_ctx* ctx, float* d_w, void* d_g, in
  * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm
  * kernel followed by the fused clip+AdamW kernel -- or, where adamw_clip_step
  * would take the one-launch step (see adamw_set_launch_options), that step
- * as one cooperative kernel node -- with the same results bit for bit as
+ * as one kernel node (a cluster or a cooperative grid, as there) -- with
+ * the same results bit for bit as
  * adamw_clip_step, and instantiates it; the context owns it (replaced by the
  * next adamw_graph_create, freed by adamw_graph_destroy or adamw_destroy).
  * adamw_graph_step writes step t's scalars (t, lr, wd, clip; bias
@@ -337,12 +338,14 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * instrumentation event between the kernels also implies plain order.)
  * States of up to 2^19 parameters (float32 gradient, 16-byte aligned arrays,
  * no weight copy, no per-tensor norms, no global_sumsq) take the whole step
- * as one cooperative launch instead (a cooperative kernel node when the
- * stream is being captured): the same
- * partial sums, the same fixed-order total and the same update, so the same
- * bits, at half the launch cost.  Its blocks meet at a grid barrier whose
- * wait is bounded (about one second); a wait that runs out skips the update
- * and makes the next adamw_last_norm return ADAMW_ECUDA.
+ * as one launch instead (one kernel node when the stream is being
+ * captured): the same partial sums, the same fixed-order total and the same
+ * update, so the same bits, at half the launch cost.  Up to 65,536
+ * parameters the launch is one thread-block cluster of 8 CTAs that meet at
+ * the cluster's hardware barrier; above, a cooperative grid whose blocks
+ * meet at a grid barrier with a bounded wait (about one second) -- a wait
+ * that runs out skips the update and makes the next adamw_last_norm return
+ * ADAMW_ECUDA.
  * ADAMW_LAUNCH_NO_ONEPASS always uses the two launches.
  * From 2^24 parameters up, the fused kernel and the checkpoint pack hand
  * their chunks out by an atomic counter, so a block that starts late (its
@@ -350,8 +353,10 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * end; the results are the same bits.  ADAMW_LAUNCH_STATIC_CHUNKS deals
  * chunks out cyclically by block at every size.
  * ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT (for tests of that path): the next
- * one-launch step waits for one block more than it launched, so its barrier
- * runs out after about a second, as above.  Used once, then cleared.
+ * one-launch step runs as the cooperative grid at any one-launch size (in a
+ * step graph: above 65,536 parameters, where the node is that grid) and
+ * waits for one block more than it launched, so its barrier runs out after
+ * about a second, as above.  Used once, then cleared.
  */
 ADAMW_API int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags);
 

@@ -1,6 +1,6 @@
 // graph.cu -- one optimizer step as a CUDA graph (norm kernel node, then the
 // fused clip+AdamW node; for states the one-launch step serves, that step as
-// one cooperative node) for states small enough that launch latency
+// one node: a cluster, or a cooperative grid) for states small enough that launch latency
 // dominates.  The per-step scalars (bias corrections depend on t) are kernel
 // arguments, so each step rewrites the two nodes' parameters in the
 // instantiated graph (cudaGraphExecKernelNodeSetParams, which leaves launches
@@ -106,9 +106,10 @@ int graph_build(adamw_ctx* ctx)
         else if ((e = cudaGraphAddKernelNode(&ctx->graph_norm, ctx->graph, nullptr, 0, &op)) !=
                  cudaSuccess)
             rc = cuda_fail(e, "cudaGraphAddKernelNode(one-launch step)");
-        else if ((e = cudaGraphKernelNodeSetAttribute(ctx->graph_norm,
+        else if (!onepass_is_cluster(ctx->n) &&  // a cluster node needs no attribute
+                 (e = cudaGraphKernelNodeSetAttribute(ctx->graph_norm,
                                                       cudaLaunchAttributeCooperative, &coop)) !=
-                 cudaSuccess)
+                     cudaSuccess)
             rc = cuda_fail(e, "cudaGraphKernelNodeSetAttribute(cooperative)");
         else if ((e = cudaGraphInstantiate(&ctx->graph_exec, ctx->graph, 0)) != cudaSuccess)
             rc = cuda_fail(e, "cudaGraphInstantiate");

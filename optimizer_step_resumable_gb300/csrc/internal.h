@@ -118,6 +118,12 @@ int launch_adamw(float* w, const void* g, float* m, float* v, int64_t n,
 // uint32 barrier counters; fault_test: wait for one block more than the grid
 // has (the barrier times out).  w, g, m, v 16-byte aligned, float32 g.
 int query_onepass_blocks(int sm_count, int* blocks_out);
+// States of at most kClusterMaxN parameters (a norm partition of at most
+// kClusterCtas blocks) take the one-launch step as one thread-block cluster
+// with a hardware barrier instead of a cooperative grid (onepass.cu).
+constexpr int kClusterCtas = 8;
+constexpr int64_t kClusterMaxN = int64_t(kClusterCtas) * kNormTileElems;
+bool onepass_is_cluster(int64_t n);
 int onepass_grid(int64_t n, int capacity);
 int launch_onepass(float* w, float* g, float* m, float* v, int64_t n, const StepScalars& k,
                    double clip, double grad_scale, double* partials, uint32_t* bar,

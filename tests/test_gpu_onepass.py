@@ -59,8 +59,11 @@ def test_same_bits_as_two_launches(dev, n):
     assert a[2] == b[2]
 
 
-def test_same_bits_with_flags_zero_grad_and_scale(dev):
-    sizes = [3, 1000, 29, 40_000, 1, 7, 24_533]
+@pytest.mark.parametrize("last", [24_533, 24_496])
+def test_same_bits_with_flags_zero_grad_and_scale(dev, last):
+    """65,573 parameters: the cooperative grid; 65,536: a cluster size, where
+    zero_grad takes the grid form (the cluster form never zeroes g)."""
+    sizes = [3, 1000, 29, 40_000, 1, 7, last]
     num = np.array(sizes, np.int64)
     off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
     n = int(num.sum())
@@ -72,12 +75,13 @@ def test_same_bits_with_flags_zero_grad_and_scale(dev):
     assert all(gb == bytes(4 * n) for gb in a[2])  # zero_grad wrote zeros
 
 
-def test_barrier_timeout_is_reported_and_the_context_recovers(dev):
+@pytest.mark.parametrize("n", [40_000, 65_573])
+def test_barrier_timeout_is_reported_and_the_context_recovers(dev, n):
     """Made to wait for one block more than it launched, the grid's bounded
     wait runs out (about a second): the step is skipped, adamw_last_norm
     reports ADAMW_ECUDA once, and the next steps match a run that never
-    faulted."""
-    n = 65_573
+    faulted.  At 40,000 parameters the test flag takes the cooperative grid
+    and the step after it the cluster form."""
     hw, hm, hv = inputs(n)
     w, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hm, hv))
     g = torch.from_numpy(synthetic.grads(7, 1, 1e-2, n=n)).to(dev)
@@ -187,7 +191,7 @@ def test_step_graph_one_node_matches_plain_steps(dev):
 
 
 def test_step_graph_barrier_timeout_is_reported(dev):
-    n = 40_000
+    n = 100_003  # a cooperative-grid node (up to 65,536 the node is a cluster: no timeout)
     hw, hm, hv = inputs(n)
     w, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hm, hv))
     g = torch.from_numpy(synthetic.grads(7, 1, 1e-2, n=n)).to(dev)
@@ -204,3 +208,58 @@ def test_step_graph_barrier_timeout_is_reported(dev):
         osr.adamw_last_norm(ctx)
         assert not torch.equal(w, torch.from_numpy(hw).to(dev))
         osr.adamw_graph_destroy(ctx)
+
+
+def test_cluster_step_graph_ignores_the_timeout_flag(dev):
+    """Up to 65,536 parameters the graph's node is the cluster kernel, which
+    has no software barrier: the test flag is consumed and the step runs
+    normally, with the two-launch step's bits."""
+    n = 40_000
+    hw, hm, hv = inputs(n)
+    hg = synthetic.grads(7, 1, 1e-2, n=n)
+    w, g, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv))
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_graph_create(ctx, w, g, m, v)
+        osr.adamw_set_launch_options(ctx, osr.LAUNCH_TEST_BARRIER_TIMEOUT)
+        osr.adamw_graph_step(ctx, 1, LR, WD, CLIP)
+        got_norm = osr.adamw_last_norm(ctx)
+        got = [x.cpu().numpy().tobytes() for x in (w, m, v)]
+    w2, g2, m2, v2 = (torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv))
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS)
+        osr.adamw_clip_step(ctx, w2, g2, m2, v2, 1, LR, WD, CLIP)
+        assert osr.adamw_last_norm(ctx) == got_norm
+    assert got == [x.cpu().numpy().tobytes() for x in (w2, m2, v2)]
+
+
+@pytest.mark.parametrize("sizes", [[3, 1000, 29, 40_000, 1, 7, 24_496], [5, 39_998]])
+def test_cluster_form_with_flags_same_bits(dev, sizes):
+    """The cluster form (no zero_grad) with decay flags, a gradient scale and
+    a ragged n % 4 tail, eager and in the step graph, against two launches."""
+    num = np.array(sizes, np.int64)
+    off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
+    n = int(num.sum())
+    mask = [k % 2 for k in range(len(sizes))]
+    kw = dict(mask=mask, grad_scale=0.25, table=(off, num))
+    a = run(dev, n, 0, **kw)
+    b = run(dev, n, osr.LAUNCH_NO_ONEPASS, **kw)
+    assert a == b
+    hw, hm, hv = inputs(n)
+    hg = synthetic.grads(7, 1, 1e-2, n=n, outlier_frac=0.01, outlier_mult=100.0)
+    outs = []
+    for use_graph in (False, True):
+        w, g, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv))
+        with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+            osr.adamw_set_decay_mask(ctx, mask)
+            if use_graph:
+                osr.adamw_graph_create(ctx, w, g, m, v)
+            else:
+                osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS)
+            for t in range(1, 4):
+                if use_graph:
+                    osr.adamw_graph_step(ctx, t, LR, WD, CLIP)
+                else:
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, LR, WD, CLIP)
+            outs.append(([x.cpu().numpy().tobytes() for x in (w, m, v)],
+                         osr.adamw_last_norm(ctx)))
+    assert outs[0] == outs[1]
