@@ -173,3 +173,8 @@ def test_read_range_bounds_and_full_range(dev, tmp_path):
     for a, b in zip((pw, pm, pv), before):  # untouched on failure
         assert torch.equal(a, b)
     part.close()
+    nock = osr.adamw_create(10, flags=osr.CREATE_NO_CKPT)  # no staging to read through
+    with pytest.raises(osr.AdamWError) as e:
+        osr.ckpt_read_range(nock, path, 0, pw, pm, pv)
+    assert e.value.status == osr.ESTATE
+    nock.close()
