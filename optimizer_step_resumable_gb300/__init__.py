@@ -166,8 +166,10 @@ def _stream(stream):
 
 
 def _same_device(t, name: str, ctx) -> None:
-    if ctx is not None and ctx.device is not None and t.device.index != ctx.device:
-        raise ValueError(f"{name} is on cuda:{t.device.index}, the context on cuda:{ctx.device}")
+    if ctx is not None and ctx.device is not None:
+        d = t.get_device()
+        if d != ctx.device:
+            raise ValueError(f"{name} is on cuda:{d}, the context on cuda:{ctx.device}")
 
 
 def _dev_ptr(t, n: int, name: str, ctx=None) -> int:

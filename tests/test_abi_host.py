@@ -176,7 +176,7 @@ def test_binding_refuses_tensors_of_another_device():
     another GPU would give the kernels an address of the wrong memory)."""
     import types
     ctx = types.SimpleNamespace(device=0)
-    on = lambda i: types.SimpleNamespace(device=types.SimpleNamespace(index=i))  # noqa: E731
+    on = lambda i: types.SimpleNamespace(get_device=lambda: i)  # noqa: E731
     osr._same_device(on(0), "w", ctx)
     osr._same_device(on(1), "w", None)  # no context: nothing to compare
     with pytest.raises(ValueError, match="cuda:1, the context on cuda:0"):
