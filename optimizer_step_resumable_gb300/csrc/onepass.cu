@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(kNormThreads, 4)
     if (ok) {
         const double s = normdev::sum_partials(partials, P);
         if (tid == 0) {
-            const NormResult r = normdev::make_result(s, clip, grad_scale, d_res->seq + 1u);
+            // only block 0 publishes, so only it reads the record's sequence number
+            const NormResult r = normdev::make_result(
+                s, clip, grad_scale, blockIdx.x == 0 ? d_res->seq + 1u : 0u);
             s_scale = r.scale;
             s_skip = r.nonfinite;
             if (blockIdx.x == 0)
@@ -236,7 +238,9 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kNormThre
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
     const double s = normdev::sum_partials(mine, P);
     if (tid == 0) {
-        const NormResult r = normdev::make_result(s, clip, grad_scale, d_res->seq + 1u);
+        // only block 0 publishes, so only it reads the record's sequence number
+        const NormResult r =
+            normdev::make_result(s, clip, grad_scale, blockIdx.x == 0 ? d_res->seq + 1u : 0u);
         s_scale = r.scale;
         s_skip = r.nonfinite;
         if (blockIdx.x == 0)

@@ -50,3 +50,26 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched like the multi-GPU bench (torchrun, 2 ranks): rank 0 alone
+    times the oracle and prints; the other rank exits 0 without output."""
+    r = subprocess.run(
+        [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+         "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+         "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1",
+         "--cpu-seconds", "0.25", "--workload", "flat-65536"],
+        cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
