@@ -615,8 +615,17 @@ ADAMW_API int ckpt_read_range(adamw_ctx* ctx, const char* path, int64_t offset,
                               int32_t* step_out, float* d_w, float* d_m, float* d_v,
                               void* stream);
 
-/* SHA-256 (FIPS 180-4) of `bytes` bytes as 64 lowercase hex digits + NUL. */
+/*
+ * SHA-256 (FIPS 180-4) of `bytes` bytes as 64 lowercase hex digits + NUL.
+ * Every digest of the library (shard files, manifests' checks) is computed
+ * by the system's libcrypto (OpenSSL 3, the CPU's SHA instructions) when it
+ * can be loaded at run time, else by the library's own implementation of
+ * the standard; both give the same digest.  OSR_SHA256=builtin in the
+ * environment, read once at the first digest, selects the library's own.
+ * ckpt_sha256_backend: 1 if libcrypto computes the digests, 0 if not.
+ */
 ADAMW_API int ckpt_sha256_hex(const void* data, int64_t bytes, char* hex_out);
+ADAMW_API int ckpt_sha256_backend(void);
 
 /* Name of a status code, and the last failure's explanation (this thread). */
 ADAMW_API const char* adamw_strerror(int status);

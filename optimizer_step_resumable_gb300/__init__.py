@@ -103,6 +103,7 @@ SIGNATURES = {
     "ckpt_read_range": (_c.c_int, [_vp, _c.c_char_p, _c.c_int64, _c.POINTER(_c.c_int32), _vp,
                                    _vp, _vp, _vp]),
     "ckpt_sha256_hex": (_c.c_int, [_vp, _c.c_int64, _c.c_char_p]),
+    "ckpt_sha256_backend": (_c.c_int, []),
     "adamw_strerror": (_c.c_char_p, [_c.c_int]),
     "adamw_last_error": (_c.c_char_p, []),
 }
@@ -564,6 +565,12 @@ def ckpt_probe(path: str, n_expected: int = -1):
                               ctypes.byref(n))
     _check(st, "ckpt_probe")
     return step.value, n.value
+
+
+def ckpt_sha256_backend() -> str:
+    """Which code computes the library's SHA-256 digests: "libcrypto" (the
+    system's OpenSSL 3) or "builtin"."""
+    return "libcrypto" if library().ckpt_sha256_backend() == 1 else "builtin"
 
 
 def ckpt_sha256_hex(data: bytes) -> str:

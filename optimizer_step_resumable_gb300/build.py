@@ -74,7 +74,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         sys.stderr.write("".join(logs))
     tmp = LIBRARY + ".part"
-    _run([nvcc(), *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs]])
+    _run([nvcc(), *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-ldl"])
     os.replace(tmp, LIBRARY)
     return LIBRARY
 

@@ -32,15 +32,27 @@ int write_named_file(const char* dir, const char* name, const IoPiece* pieces, i
 // Deletes all but the `keep` newest step_<digits>.bin files of dir.
 int rotate_files(const char* dir, int32_t keep, int32_t* removed);
 
-// SHA-256 (FIPS 180-4), incremental (sha256.cpp).
+// SHA-256 (FIPS 180-4), incremental (sha256.cpp).  The digest is computed
+// by the system's libcrypto (OpenSSL 3, which uses the CPU's SHA
+// instructions) when it can be loaded, else by the library's own code from
+// the standard; both give the same digest.  OSR_SHA256=builtin in the
+// environment (read once, at the first digest) selects the library's own.
 class Sha256 {
 public:
     Sha256() { reset(); }
+    ~Sha256();
+    Sha256(const Sha256&) = delete;
+    Sha256& operator=(const Sha256&) = delete;
     void reset();
     void update(const void* data, size_t bytes);
-    void final_hex(char out[65]);  // 64 lowercase hex digits + NUL
+    // 64 lowercase hex digits + NUL; false if libcrypto reported an error
+    // (out is then not a digest).
+    bool final_hex(char out[65]);
+    static bool uses_libcrypto();
 
 private:
+    void* evp_ = nullptr;  // libcrypto's digest context, or NULL: own code
+    bool evp_failed_ = false;
     uint32_t h_[8];
     uint64_t len_;
     unsigned char buf_[64];

@@ -430,7 +430,10 @@ int load_manifest(const char* step_dir, int32_t expected_world, bool verify, int
                 h.update(chunk.data(), size_t(got));
             }
             char hex[65];
-            h.final_hex(hex);
+            if (!h.final_hex(hex)) {
+                ::close(sfd);
+                return fail(ADAMW_EIO, "%s: the digest could not be computed", sp.c_str());
+            }
             if ((*digests)[size_t(r)] != hex) {
                 ::close(sfd);
                 return fail(ADAMW_EFORMAT, "%s: sha256 %s, manifest says %s (partial or corrupted "
@@ -475,7 +478,8 @@ int ckpt_shard_write_host(const char* dir, int32_t step, int32_t rank, int32_t n
     osr::Sha256 h;
     for (const auto& p : pieces)
         h.update(p.data, p.bytes);
-    h.final_hex(sha256_hex_out);
+    if (!h.final_hex(sha256_hex_out))
+        return osr::fail(ADAMW_EIO, "rank%d.bin: the digest could not be computed", int(rank));
     return ADAMW_OK;
 }
 
@@ -684,8 +688,9 @@ int ckpt_consolidate(const char* step_dir, int32_t expected_world, const char* o
     close_all();
     for (size_t r = 0; r < world && rc == ADAMW_OK; ++r) {
         char hex[65];
-        hashes[r].final_hex(hex);
-        if (digests[r] != hex)
+        if (!hashes[r].final_hex(hex))
+            rc = osr::fail(ADAMW_EIO, "%s: the digest could not be computed", spaths[r].c_str());
+        else if (digests[r] != hex)
             rc = osr::fail(ADAMW_EFORMAT, "%s: sha256 %s, manifest says %s (partial or corrupted "
                            "write)", spaths[r].c_str(), hex, digests[r].c_str());
     }

@@ -1,10 +1,19 @@
 // sha256.cpp -- SHA-256 (FIPS PUB 180-4, "Secure Hash Standard", section
-// 6.2), portable C++, for the shard digests of the sharded checkpoint's
-// manifest.  Written from the standard's description: 512-bit blocks, a
-// 64-word message schedule, 64 rounds with the functions Ch, Maj, Sigma0/1
-// and sigma0/1, the big-endian length padding of section 5.1.1.
+// 6.2) for the shard digests of the sharded checkpoint's manifest.
+//
+// Two backends with one result.  The system's libcrypto (OpenSSL 3), loaded
+// at run time through its public EVP digest interface, hashes with the CPU's
+// SHA instructions: about 1.3 GB/s on one x86 core against 160 MB/s for
+// portable code, which for a 1.33 GB shard is 1 s instead of 8.  When it
+// cannot be loaded (or OSR_SHA256=builtin), the library's own portable code
+// runs, written from the standard's description: 512-bit blocks, a 64-word
+// message schedule, 64 rounds with the functions Ch, Maj, Sigma0/1 and
+// sigma0/1, the big-endian length padding of section 5.1.1.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
+
+#include <dlfcn.h>
 
 #include "ckpt_io.h"
 #include "internal.h"
@@ -71,17 +80,79 @@ void compress(uint32_t h[8], const unsigned char* block)
     h[7] += k;
 }
 
+// libcrypto's EVP digest interface (public OpenSSL 3 API), resolved once.
+struct Evp {
+    void* (*ctx_new)() = nullptr;
+    void (*ctx_free)(void*) = nullptr;
+    const void* (*sha256)() = nullptr;
+    int (*init)(void*, const void*, void*) = nullptr;
+    int (*update)(void*, const void*, size_t) = nullptr;
+    int (*final)(void*, unsigned char*, unsigned int*) = nullptr;
+    bool ok = false;
+};
+
+template <typename F>
+bool resolve(void* lib, const char* name, F* out)
+{
+    *out = reinterpret_cast<F>(::dlsym(lib, name));
+    return *out != nullptr;
+}
+
+const Evp& evp()
+{
+    static const Evp e = [] {
+        Evp r;
+        const char* choice = std::getenv("OSR_SHA256");
+        if (choice && std::strcmp(choice, "builtin") == 0)
+            return r;
+        void* lib = ::dlopen("libcrypto.so.3", RTLD_NOW | RTLD_LOCAL);
+        if (!lib)
+            return r;  // kept open for the life of the process once found
+        r.ok = resolve(lib, "EVP_MD_CTX_new", &r.ctx_new) &&
+               resolve(lib, "EVP_MD_CTX_free", &r.ctx_free) &&
+               resolve(lib, "EVP_sha256", &r.sha256) &&
+               resolve(lib, "EVP_DigestInit_ex", &r.init) &&
+               resolve(lib, "EVP_DigestUpdate", &r.update) &&
+               resolve(lib, "EVP_DigestFinal_ex", &r.final) && r.sha256() != nullptr;
+        return r;
+    }();
+    return e;
+}
+
 }  // namespace
+
+bool Sha256::uses_libcrypto() { return evp().ok; }
+
+Sha256::~Sha256()
+{
+    if (evp_)
+        evp().ctx_free(evp_);
+}
 
 void Sha256::reset()
 {
     std::memcpy(h_, kInit, sizeof h_);
     len_ = 0;
     fill_ = 0;
+    evp_failed_ = false;
+    const Evp& e = evp();
+    if (!e.ok)
+        return;
+    if (!evp_)
+        evp_ = e.ctx_new();
+    if (evp_ && e.init(evp_, e.sha256(), nullptr) != 1) {  // own code instead
+        e.ctx_free(evp_);
+        evp_ = nullptr;
+    }
 }
 
 void Sha256::update(const void* data, size_t bytes)
 {
+    if (evp_) {
+        if (bytes > 0 && evp().update(evp_, data, bytes) != 1)
+            evp_failed_ = true;
+        return;
+    }
     const unsigned char* p = static_cast<const unsigned char*>(data);
     len_ += bytes;
     if (fill_) {
@@ -101,26 +172,35 @@ void Sha256::update(const void* data, size_t bytes)
     fill_ = bytes;
 }
 
-void Sha256::final_hex(char out[65])
+bool Sha256::final_hex(char out[65])
 {
-    // padding: a 1 bit, zeros, then the message length in bits, big-endian
-    const uint64_t bits = len_ * 8u;
-    const unsigned char one = 0x80, zero = 0x00;
-    update(&one, 1);
-    while (fill_ != 56)
-        update(&zero, 1);
-    unsigned char lenbe[8];
-    for (int i = 0; i < 8; ++i)
-        lenbe[i] = static_cast<unsigned char>(bits >> (56 - 8 * i));
-    update(lenbe, 8);
+    unsigned char digest[32];
+    bool ok = true;
+    if (evp_) {
+        unsigned int len = 0;
+        ok = !evp_failed_ && evp().final(evp_, digest, &len) == 1 && len == 32;
+    } else {
+        // padding: a 1 bit, zeros, then the message length in bits, big-endian
+        const uint64_t bits = len_ * 8u;
+        const unsigned char one = 0x80, zero = 0x00;
+        update(&one, 1);
+        while (fill_ != 56)
+            update(&zero, 1);
+        unsigned char lenbe[8];
+        for (int i = 0; i < 8; ++i)
+            lenbe[i] = static_cast<unsigned char>(bits >> (56 - 8 * i));
+        update(lenbe, 8);
+        for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 4; ++j)
+                digest[4 * i + j] = static_cast<unsigned char>((h_[i] >> (24 - 8 * j)) & 0xffu);
+    }
     static const char hex[] = "0123456789abcdef";
-    for (int i = 0; i < 8; ++i)
-        for (int j = 0; j < 4; ++j) {
-            const unsigned byte = (h_[i] >> (24 - 8 * j)) & 0xffu;
-            out[8 * i + 2 * j] = hex[byte >> 4];
-            out[8 * i + 2 * j + 1] = hex[byte & 15];
-        }
+    for (int i = 0; i < 32; ++i) {
+        out[2 * i] = ok ? hex[digest[i] >> 4] : '0';
+        out[2 * i + 1] = ok ? hex[digest[i] & 15] : '0';
+    }
     out[64] = '\0';
+    return ok;
 }
 
 }  // namespace osr
@@ -132,6 +212,9 @@ extern "C" int ckpt_sha256_hex(const void* data, int64_t bytes, char* hex_out)
         return osr::fail(ADAMW_EINVAL, "ckpt_sha256_hex: bad arguments");
     osr::Sha256 s;
     s.update(data, size_t(bytes));
-    s.final_hex(hex_out);
+    if (!s.final_hex(hex_out))
+        return osr::fail(ADAMW_EIO, "ckpt_sha256_hex: libcrypto reported an error");
     return ADAMW_OK;
 }
+
+extern "C" int ckpt_sha256_backend(void) { return osr::Sha256::uses_libcrypto() ? 1 : 0; }

@@ -235,7 +235,8 @@ int ckpt_shard_write(adamw_ctx* ctx, const char* dir, int32_t rank, char* sha256
         return rc;
     osr::Sha256 h;
     h.update(ctx->h_image(), ctx->image_bytes());
-    h.final_hex(sha256_hex_out);
+    if (!h.final_hex(sha256_hex_out))
+        return osr::fail(ADAMW_EIO, "%s: the digest could not be computed", name);
     return ADAMW_OK;
 }
 
@@ -287,7 +288,8 @@ int ckpt_shard_read(adamw_ctx* ctx, const char* step_dir, int32_t rank, int32_t 
     char hex[65];
     osr::Sha256 h;
     h.update(img, ctx->image_bytes());
-    h.final_hex(hex);
+    if (!h.final_hex(hex))
+        return osr::fail(ADAMW_EIO, "%s: the digest could not be computed", path.c_str());
     if (digests[size_t(rank)] != hex)
         return osr::fail(ADAMW_EFORMAT, "%s: sha256 %s, manifest says %s (partial or corrupted "
                          "write)", path.c_str(), hex, digests[size_t(rank)].c_str());

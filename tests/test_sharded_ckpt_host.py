@@ -36,6 +36,34 @@ def test_sha256_matches_hashlib(lib):
         assert osr.ckpt_sha256_hex(data) == hashlib.sha256(data).hexdigest(), size
 
 
+def test_sha256_builtin_backend_matches_hashlib(lib):
+    """The library's own SHA-256 (forced with OSR_SHA256=builtin, in a fresh
+    process) against the standard's vectors and hashlib on odd lengths --
+    the code that runs where libcrypto cannot be loaded."""
+    import subprocess
+    import sys
+    code = (
+        "import hashlib, sys, numpy as np\n"
+        "sys.path.insert(0, %r)\n"
+        "import optimizer_step_resumable_gb300 as osr\n"
+        "assert osr.ckpt_sha256_backend() == 'builtin'\n"
+        "assert osr.ckpt_sha256_hex(b'abc') == "
+        "'ba7816bf8f01cfea414140de5dae2223b00361a396177a9cb410ff61f20015ad'\n"
+        "rng = np.random.default_rng(1)\n"
+        "for size in list(range(0, 130)) + [1023, 65537, 1 << 20]:\n"
+        "    d = rng.integers(0, 256, size, dtype=np.uint8).tobytes()\n"
+        "    assert osr.ckpt_sha256_hex(d) == hashlib.sha256(d).hexdigest(), size\n"
+        "print('ok')\n") % ROOT
+    env = dict(os.environ, OSR_SHA256="builtin")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr[-2000:]
+
+
+def test_sha256_backend_is_reported(lib):
+    assert osr.ckpt_sha256_backend() in ("libcrypto", "builtin")
+
+
 def _shards(sizes, seed=3):
     rng = np.random.default_rng(seed)
     return [tuple(rng.standard_normal(k).astype(np.float32) for _ in range(3)) for k in sizes]
