@@ -341,10 +341,11 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * as one launch instead (one kernel node when the stream is being
  * captured): the same partial sums, the same fixed-order total and the same
  * update, so the same bits, at half the launch cost.  Up to 65,536
- * parameters the launch is one thread-block cluster of 8 CTAs that meet at
- * the cluster's hardware barrier; above, a cooperative grid whose blocks
- * meet at a grid barrier with a bounded wait (about one second) -- a wait
- * that runs out skips the update and makes the next adamw_last_norm return
+ * parameters (without ADAMW_ZERO_GRAD) the launch is thread-block clusters
+ * of 8 CTAs, each cluster computing the norm itself and meeting at its
+ * hardware barrier; otherwise a cooperative grid whose blocks meet at a
+ * grid barrier with a bounded wait (about one second) -- a wait that runs
+ * out skips the update and makes the next adamw_last_norm return
  * ADAMW_ECUDA.
  * ADAMW_LAUNCH_NO_ONEPASS always uses the two launches.
  * From 2^24 parameters up, the fused kernel and the checkpoint pack hand
