@@ -124,10 +124,12 @@ ADAMW_API int adamw_create(int64_t n_params, const int64_t* offsets,
  * NULL is accepted. */
 ADAMW_API int adamw_destroy(adamw_ctx* ctx);
 
-/* Replaces beta1, beta2 (each in [0, 1)) and eps (>= 0). */
+/* Replaces beta1, beta2 (each in [0, 1)) and eps (finite, >= 0) for the
+ * following steps (the step graph's included); ADAMW_EINVAL otherwise, the
+ * previous values kept.  The defaults are the pages' 0.9, 0.999, 1e-8. */
 ADAMW_API int adamw_set_hparams(adamw_ctx* ctx, double beta1, double beta2, double eps);
 
-/* Number of parameters and tensors of the context. */
+/* Number of parameters and tensors of the context; -1 for a NULL ctx. */
 ADAMW_API int64_t adamw_num_params(const adamw_ctx* ctx);
 ADAMW_API int32_t adamw_num_tensors(const adamw_ctx* ctx);
 
