@@ -147,3 +147,44 @@ def test_misaligned_16bit_refused(dev):
         with pytest.raises(osr.AdamWError) as e:
             osr.adamw_clip_step_mixed(ctx, w, buf[1:n + 1], m, v, 1, 1e-3, 0.0, 1.0)
         assert e.value.status == osr.EINVAL
+
+
+def test_full_size_bf16_copy_zero_grad_sampled(dev, oracle):
+    """The 110M tensor list (chunks handed out by the counter at this size)
+    with a bfloat16 gradient, a bfloat16 weight copy and zero_grad: the norm
+    within 1e-6 of the oracle's, sampled elements within the one-step bar,
+    the copy the exact rounding of the new weights there, and g zeroed."""
+    from parity import assert_state_close, sample_indices
+    from synthetic import device as synth_dev
+    from synthetic import workloads as W
+    wl = W.gpt_110m()
+    n = wl.n
+    off, num = wl.table()
+    w = torch.empty(n, device=dev)
+    synth_dev.fill_weights(w, wl.seed)
+    g32 = torch.empty(n, device=dev)
+    synth_dev.fill_grads(g32, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
+    hw = w.cpu().numpy().copy()
+    gb = bits16(g32.cpu().numpy(), 1)  # rounded on the host, uploaded as bits
+    del g32
+    g = upload16(gb, 1, dev)
+    m, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    w_lp = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_clip_step_mixed(ctx, w, g, m, v, 1, wl.lr, wl.wd, wl.clip, w_lp=w_lp,
+                                  zero_grad=True)
+        norm, _ = osr.adamw_last_norm(ctx)
+    gd = decode(gb, 1)
+    onorm = oracle.global_norm(gd)
+    assert abs(norm - onorm) <= RTOL_NORM * onorm
+    s = oracle.clip_scale(onorm, wl.clip)
+    idx = sample_indices(n, 200_000)
+    zeros = np.zeros(n, np.float32)
+    want = oracle.adamw_at(idx, hw, gd, zeros, zeros, s, 1, wl.lr, wl.wd)
+    terms = oracle.adamw_terms_at(idx, hw, gd, zeros, zeros, s, 1, wl.lr, wl.wd)
+    ti = torch.from_numpy(idx).to(dev)
+    got = [x[ti].cpu().numpy() for x in (w, m, v)]
+    assert_state_close(got, want, terms, RTOL_ONE_STEP, "110M bf16", lr=wl.lr, t=1)
+    lp = w_lp.view(torch.int16)[ti].cpu().numpy().view(np.uint16)
+    assert lp.tobytes() == bits16(got[0], 1).tobytes()
+    assert not bool(g.view(torch.int16).any())
