@@ -25,8 +25,11 @@ def _state(dev, n, offset=0):
     return w, g, m, v
 
 
-@pytest.mark.parametrize("n,offset", [(65536, 0), (1_000_003, 0), (40_001, 1)])
+@pytest.mark.parametrize("n,offset", [(65536, 0), (1_000_003, 0), (40_001, 1),
+                                      ((1 << 24) + 5, 0)])
 def test_graph_steps_equal_plain_steps(dev, n, offset):
+    """(2^24 + 5: the fused node hands chunks out by its counter, which must
+    reset itself for every replay.)"""
     a = _state(dev, n, offset)
     b = _state(dev, n, offset)
     sched = [(t, 3e-3 * (0.5 if t > 20 else 1.0), 0.01, 1.0 if t % 7 else 0.5) for t in range(1, 41)]
