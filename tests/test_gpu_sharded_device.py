@@ -38,9 +38,10 @@ def shards(dev, n, world):
 
 
 # every world size at both sizes for a float32 gradient; one size suffices
-# for the 16-bit gradient
+# for the 16-bit gradient; one shard of 2^24 + 5 parameters takes the
+# counter-scheduled chunks behind both exchanges
 CASES = ([(w, n, "f32") for w in (1, 2, 3, 4) for n in (65_573, 1_000_003)] +
-         [(w, 1_000_003, "bf16") for w in (1, 2, 3, 4)])
+         [(w, 1_000_003, "bf16") for w in (1, 2, 3, 4)] + [(1, (1 << 24) + 5, "f32")])
 
 
 @pytest.mark.parametrize("world,n,gdt", CASES)
