@@ -35,8 +35,10 @@ def _close(a, b, rtol):
     return bool(np.all(np.abs(a - b) <= bound))
 
 
-@pytest.mark.parametrize("n", [65536 + 37, 1_000_003])
+@pytest.mark.parametrize("n", [65536 + 37, 1_000_003, (1 << 24) + 5])
 def test_noalloc_step_matches_context_step(dev, n):
+    """(2^24 + 5: the context step hands chunks out by its counter, the
+    no-alloc step keeps the fixed assignment.)"""
     w0 = torch.from_numpy(synthetic.weights(7, n=n)).to(dev)
     states = [[w0.clone(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)]
               for _ in range(2)]
