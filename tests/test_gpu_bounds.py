@@ -46,8 +46,9 @@ class Guarded:
         assert now[hi:] == self.before[hi:], "write past the array"
 
 
+# (from 2^24 the fused and pack kernels hand chunks out by their counters)
 SIZES = [1, 2, 3, 4, 5, 7, 8, 9, 31, 33, 1023, 1025, 2047, 2049, 8191, 8193,
-         65537, (1 << 19) - 1, (1 << 19) + 3, 3 * 8192 * 608 + 5]
+         65537, (1 << 19) - 1, (1 << 19) + 3, 3 * 8192 * 608 + 5, (1 << 24) + 2, (1 << 24) + 5]
 
 
 @pytest.mark.parametrize("n", SIZES)
@@ -75,7 +76,8 @@ def test_step_paths_stay_in_bounds(dev, n, offset):
         a.check()
 
 
-@pytest.mark.parametrize("n", [1, 3, 4, 5, 9, 2049, 8193, 65537, (1 << 19) + 3])
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 9, 2049, 8193, 65537, (1 << 19) + 3,
+                               (1 << 24) + 3])
 def test_mixed_paths_stay_in_bounds(dev, n):
     w = Guarded(dev, n, fill=0.5)
     m = Guarded(dev, n)
