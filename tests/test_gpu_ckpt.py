@@ -32,7 +32,7 @@ def state(dev, n, seed=7):
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9, 1001, 65536, 65536 + 2,
-                               1_000_001, 1_000_003])
+                               1_000_001, 1_000_003, (1 << 24) + 3])
 @pytest.mark.parametrize("copy", ["kernel", "copy_engine"])
 def test_pack_write_bytes_match_oracle(dev, oracle, tmp_path, n, copy):
     """Both ways from the staging to the pinned image (the side-stream
