@@ -256,6 +256,42 @@ ADAMW_API int adamw_clip_step_gathered(adamw_ctx* ctx, float* d_w, void* d_g, in
                                        void* stream);
 
 /*
+ * The sharded step with the exchange on the host ("Training as a
+ * Recoverable State Transition", section "The Exact Targets of Clipping and
+ * AdamW": the clip uses the norm of all gradients joined into one vector;
+ * "Checkpoint and Sharded Resume", lesson 80, section "Manifest schema":
+ * each rank owns the contiguous range param_shard_offset /
+ * param_shard_numel).  Per step, on each rank: grad_sumsq gives the shard's
+ * sum of g^2 on the host; the caller gathers one double per rank, in rank
+ * order, into a host array (e.g. a gloo all-gather); then:
+ *
+ * adamw_rank_total (host only, no GPU needed): S = h_rank_sumsq[0] + ... +
+ *   h_rank_sumsq[world - 1], added in rank order in double (the order and
+ *   formula of the device form, adamw_clip_step_gathered, so the same bits);
+ *   norm = grad_scale sqrt(S); the factor applied to the raw gradient,
+ *   grad_scale (norm > clip ? clip / norm : 1), rounded to float once.  Each
+ *   output pointer may be NULL.  Errors: ADAMW_EINVAL (NULL array, world < 1,
+ *   a negative rank value, clip <= 0, grad_scale not finite and > 0);
+ *   ADAMW_ENONFINITE when the norm is inf or nan (outputs still stored, the
+ *   factor then grad_scale).
+ * adamw_clip_step_ranks: adamw_rank_total, then the fused update of this
+ *   rank's shard with that factor (adamw_clip_step_mixed with global_sumsq =
+ *   S; no norm kernel runs).  h_rank_sumsq is read before the call returns.
+ *   A non-finite global norm returns ADAMW_ENONFINITE with nothing
+ *   launched.  flags: ADAMW_ZERO_GRAD (ADAMW_TENSOR_NORMS is refused: the
+ *   shard's own reduction does not run).  g_dtype and alignment as
+ *   adamw_clip_step_gathered.
+ */
+ADAMW_API int adamw_rank_total(const double* h_rank_sumsq, int32_t world, double clip,
+                               double grad_scale, double* sumsq_out, double* norm_out,
+                               float* scale_out);
+ADAMW_API int adamw_clip_step_ranks(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype,
+                                    float* d_m, float* d_v, int32_t t, double lr, double wd,
+                                    double clip, double grad_scale,
+                                    const double* h_rank_sumsq, int32_t world, int32_t flags,
+                                    void* stream);
+
+/*
  * One step as a CUDA graph, for states small enough that launch latency
  * dominates (e.g. 65,536 parameters: L2-resident, a few microseconds per
  * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm

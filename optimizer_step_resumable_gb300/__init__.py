@@ -59,6 +59,12 @@ SIGNATURES = {
     "adamw_clip_step_gathered": (_c.c_int, [_vp, _vp, _vp, _c.c_int32, _vp, _vp, _c.c_int32,
                                             _c.c_double, _c.c_double, _c.c_double, _c.c_double,
                                             _vp, _c.c_int32, _c.c_int32, _vp]),
+    "adamw_rank_total": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double,
+                                    _c.POINTER(_c.c_double), _c.POINTER(_c.c_double),
+                                    _c.POINTER(_c.c_float)]),
+    "adamw_clip_step_ranks": (_c.c_int, [_vp, _vp, _vp, _c.c_int32, _vp, _vp, _c.c_int32,
+                                         _c.c_double, _c.c_double, _c.c_double, _c.c_double,
+                                         _vp, _c.c_int32, _c.c_int32, _vp]),
     "adamw_last_tensor_sumsq": (_c.c_int, [_vp, _vp]),
     "adamw_graph_create": (_c.c_int, [_vp, _vp, _vp, _vp, _vp]),
     "adamw_graph_step": (_c.c_int, [_vp, _c.c_int32, _c.c_double, _c.c_double, _c.c_double,
@@ -352,6 +358,46 @@ def adamw_clip_step_gathered(ctx: Context, w, g, m, v, t: int, lr: float, wd: fl
         float(grad_scale), _f64_dev_ptr(rank_sumsq, world, "rank_sumsq", ctx), int(world),
         ZERO_GRAD if zero_grad else 0, _stream(stream))
     _check(st, "adamw_clip_step_gathered")
+
+
+def _f64_host_array(values, name: str):
+    """The values as a C array of doubles (ctypes; the caller keeps it alive)."""
+    vals = [float(x) for x in values]
+    if not vals:
+        raise ValueError(f"{name} is empty")
+    return (_c.c_double * len(vals))(*vals), len(vals)
+
+
+def adamw_rank_total(rank_sumsq, clip: float, grad_scale: float = 1.0):
+    """(sum, norm, clip factor) of the ranks' sums of squares, added in rank
+    order by the library (host only).  Raises NonFiniteGradient (with
+    .values = (sum, norm, factor)) when the norm is inf or nan."""
+    arr, world = _f64_host_array(rank_sumsq, "rank_sumsq")
+    s, norm, scale = _c.c_double(), _c.c_double(), _c.c_float()
+    st = library().adamw_rank_total(arr, world, float(clip), float(grad_scale), _c.byref(s),
+                                    _c.byref(norm), _c.byref(scale))
+    if st == ENONFINITE:
+        err = NonFiniteGradient(st, "adamw_rank_total", adamw_last_error())
+        err.values = (s.value, norm.value, scale.value)
+        raise err
+    _check(st, "adamw_rank_total")
+    return s.value, norm.value, scale.value
+
+
+def adamw_clip_step_ranks(ctx: Context, w, g, m, v, t: int, lr: float, wd: float, clip: float,
+                          rank_sumsq, grad_scale: float = 1.0, zero_grad: bool = False,
+                          stream=None):
+    """The fused update of this shard with the global norm of the ranks'
+    sums of squares (a host sequence, one float per rank in rank order, e.g.
+    gathered over gloo), added up by the library."""
+    n = ctx.n
+    arr, world = _f64_host_array(rank_sumsq, "rank_sumsq")
+    st = library().adamw_clip_step_ranks(
+        ctx.handle, _dev_ptr(w, n, "w", ctx), _typed_ptr(g, n, "g", ctx), _dtype_of(g),
+        _dev_ptr(m, n, "m", ctx), _dev_ptr(v, n, "v", ctx), int(t), float(lr), float(wd),
+        float(clip), float(grad_scale), arr, world, ZERO_GRAD if zero_grad else 0,
+        _stream(stream))
+    _check(st, "adamw_clip_step_ranks")
 
 
 def grad_tensor_sumsq(ctx: Context, g, stream=None):

@@ -614,6 +614,56 @@ int adamw_clip_step_gathered(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dt
                      clip, grad_scale, -1.0, d_rank_sumsq, world, flags, stream);
 }
 
+int adamw_rank_total(const double* h_rank_sumsq, int32_t world, double clip, double grad_scale,
+                     double* sumsq_out, double* norm_out, float* scale_out)
+{
+    osr::clear_error();
+    if (!h_rank_sumsq || world < 1)
+        return fail(ADAMW_EINVAL, "h_rank_sumsq is NULL or world=%d < 1", world);
+    if (!(clip > 0.0))
+        return fail(ADAMW_EINVAL, "clip=%g must be > 0 (INFINITY disables clipping)", clip);
+    if (!(grad_scale > 0.0 && std::isfinite(grad_scale)))
+        return fail(ADAMW_EINVAL, "grad_scale=%g must be finite and > 0", grad_scale);
+    // rank order, one double addition per rank (the device form, the
+    // k_rank_total kernel, adds in the same order)
+    double s = 0.0;
+    for (int32_t r = 0; r < world; ++r) {
+        const double x = h_rank_sumsq[r];
+        if (x < 0.0)
+            return fail(ADAMW_EINVAL, "rank %d's sum of squares is negative (%g)", r, x);
+        s += x;
+    }
+    const double norm = grad_scale * std::sqrt(s);
+    const bool finite = std::isfinite(norm);
+    if (sumsq_out)
+        *sumsq_out = s;
+    if (norm_out)
+        *norm_out = norm;
+    if (scale_out)
+        *scale_out = float(grad_scale * ((finite && norm > clip) ? clip / norm : 1.0));
+    if (!finite)
+        return fail(ADAMW_ENONFINITE, "global gradient norm is %g", norm);
+    return ADAMW_OK;
+}
+
+int adamw_clip_step_ranks(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, float* d_m,
+                          float* d_v, int32_t t, double lr, double wd, double clip,
+                          double grad_scale, const double* h_rank_sumsq, int32_t world,
+                          int32_t flags, void* stream)
+{
+    if (flags & ADAMW_TENSOR_NORMS) {
+        osr::clear_error();
+        return fail(ADAMW_EINVAL, "per-tensor norms need the shard's own reduction");
+    }
+    double total = 0.0;
+    const int rc = adamw_rank_total(h_rank_sumsq, world, clip, grad_scale, &total, nullptr,
+                                    nullptr);
+    if (rc != ADAMW_OK)  // a non-finite global norm: nothing is launched
+        return rc;
+    return step_impl(ctx, d_w, d_g, g_dtype, d_m, d_v, nullptr, ADAMW_DTYPE_BF16, t, lr, wd,
+                     clip, grad_scale, total, nullptr, 0, flags, stream);
+}
+
 int grad_sumsq_to(adamw_ctx* ctx, const void* d_g, int32_t g_dtype, double* d_out, void* stream)
 {
     osr::clear_error();

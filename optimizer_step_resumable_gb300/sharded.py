@@ -3,17 +3,18 @@
 Each rank owns one contiguous range of the flat state (its shard of w, m, v
 and the gradient of that range).  The global clip needs the norm of the
 whole gradient, so the ranks exchange their shards' sums of squares -- one
-double each -- and add them in rank order, which makes the result the same
-on every rank and from run to run.  Each rank then runs the fused update on
-its own shard with that global sum (adamw_clip_step_ex, global_sumsq).  The
-exchange uses torch.distributed (gloo or NCCL); everything else runs in the
-library's kernels.
+double each.  The library adds them in rank order (adamw_clip_step_ranks on
+the host, adamw_clip_step_gathered on the device), which makes the result
+the same on every rank and from run to run, and runs the fused update on
+the rank's own shard with that global sum.  This module only partitions and
+exchanges (torch.distributed, gloo or NCCL); the arithmetic runs in the
+library.
 """
 from __future__ import annotations
 
 import time
 
-from . import (adamw_clip_step_ex, adamw_clip_step_gathered, ckpt_consolidate,
+from . import (adamw_clip_step_gathered, adamw_clip_step_ranks, ckpt_consolidate,
                ckpt_manifest_commit, ckpt_pack, ckpt_probe, ckpt_read_range, ckpt_shard_read,
                ckpt_shard_write, grad_sumsq, grad_sumsq_to)
 
@@ -32,20 +33,13 @@ def shard_range(n: int, rank: int, world: int, align: int = 4):
     return off, numel
 
 
-def ordered_sum(parts):
-    """Sum of the ranks' values in rank order, in double."""
-    total = 0.0
-    for x in parts:
-        total = total + float(x)
-    return total
-
-
-def global_sumsq(local: float, group=None) -> float:
-    """Every rank's local sum of squares, gathered and added in rank order."""
+def gather_sumsq(local: float, group=None) -> list:
+    """Every rank's local sum of squares, in rank order (an all-gather; the
+    library adds them up).  Without an initialised process group: [local]."""
     import torch
     import torch.distributed as dist
     if not dist.is_available() or not dist.is_initialized():
-        return float(local)
+        return [float(local)]
     world = dist.get_world_size(group)
     backend = dist.get_backend(group)
     device = (torch.device("cuda", torch.cuda.current_device())
@@ -53,18 +47,17 @@ def global_sumsq(local: float, group=None) -> float:
     mine = torch.tensor([float(local)], dtype=torch.float64, device=device)
     parts = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(parts, mine, group=group)
-    return ordered_sum(p.item() for p in parts)
+    return [p.item() for p in parts]
 
 
 def sharded_clip_step(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=1.0, zero_grad=False,
                       group=None, stream=None):
-    """One clipped-AdamW step on this rank's shard; returns the global sum
-    of squares of the raw gradient."""
-    local = grad_sumsq(ctx, g, stream=stream)
-    total = global_sumsq(local, group)
-    adamw_clip_step_ex(ctx, w, g, m, v, t, lr, wd, clip, grad_scale=grad_scale,
-                       global_sumsq=total, zero_grad=zero_grad, stream=stream)
-    return total
+    """One clipped-AdamW step on this rank's shard; returns the gathered
+    per-rank sums of squares of the raw gradient (rank order)."""
+    parts = gather_sumsq(grad_sumsq(ctx, g, stream=stream), group)
+    adamw_clip_step_ranks(ctx, w, g, m, v, t, lr, wd, clip, parts, grad_scale=grad_scale,
+                          zero_grad=zero_grad, stream=stream)
+    return parts
 
 
 class DeviceExchange:

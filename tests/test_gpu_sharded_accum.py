@@ -10,7 +10,7 @@ from parity import RTOL_NORM, RTOL_ONE_STEP, RTOL_TRAJECTORY, Running, assert_wi
 
 torch = pytest.importorskip("torch")
 import optimizer_step_resumable_gb300 as osr  # noqa: E402
-from optimizer_step_resumable_gb300.sharded import ordered_sum, shard_range  # noqa: E402
+from optimizer_step_resumable_gb300.sharded import shard_range  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -41,10 +41,9 @@ def test_virtual_shards_match_oracle(dev, oracle, world):
             g = torch.from_numpy(hg).to(dev)
             sl = [slice(o, o + k) for o, k in spans]
             parts = [osr.grad_sumsq(c, g[s]) for c, s in zip(ctxs, sl)]
-            total = ordered_sum(parts)
+            total = osr.adamw_rank_total(parts, 1.0)[0]
             for c, s in zip(ctxs, sl):
-                osr.adamw_clip_step_ex(c, w[s], g[s], m[s], v[s], t, 3e-3, 0.01, 1.0,
-                                       global_sumsq=total)
+                osr.adamw_clip_step_ranks(c, w[s], g[s], m[s], v[s], t, 3e-3, 0.01, 1.0, parts)
             onorm = oracle.global_norm(hg)
             assert abs(np.sqrt(total) - onorm) <= RTOL_NORM * onorm
             s_or = oracle.clip_scale(onorm, 1.0)

@@ -14,7 +14,7 @@ from synthetic import device as synth_dev
 
 torch = pytest.importorskip("torch")
 import optimizer_step_resumable_gb300 as osr  # noqa: E402
-from optimizer_step_resumable_gb300.sharded import ordered_sum, shard_range  # noqa: E402
+from optimizer_step_resumable_gb300.sharded import shard_range  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -29,10 +29,9 @@ def sharded_steps(ctxs, spans, w, m, v, g, t0, t1):
     for t in range(t0, t1 + 1):
         synth_dev.fill_grads(g, 7, t, 1e-2, 0.01, 100.0)
         sl = [slice(o, o + k) for o, k in spans]
-        total = ordered_sum(osr.grad_sumsq(c, g[s]) for c, s in zip(ctxs, sl))
+        parts = [osr.grad_sumsq(c, g[s]) for c, s in zip(ctxs, sl)]
         for c, s in zip(ctxs, sl):
-            osr.adamw_clip_step_ex(c, w[s], g[s], m[s], v[s], t, 3e-3, 0.01, 1.0,
-                                   global_sumsq=total)
+            osr.adamw_clip_step_ranks(c, w[s], g[s], m[s], v[s], t, 3e-3, 0.01, 1.0, parts)
 
 
 @pytest.mark.parametrize("world", [2, 4])

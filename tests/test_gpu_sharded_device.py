@@ -1,7 +1,7 @@
 """The sharded step with the exchange on the device (grad_sumsq_to, an
 all-gather, adamw_clip_step_gathered) against the host-side exchange
-(grad_sumsq, rank-order sum on the host, adamw_clip_step_ex with
-global_sumsq): the same bits, for 1 to 4 virtual ranks on one GPU (each rank
+(grad_sumsq, the gathered values handed to adamw_clip_step_ranks, which
+adds them in rank order on the host): the same bits, for 1 to 4 virtual ranks on one GPU (each rank
 one context over its shard; the all-gather is a copy of each rank's value
 into its slot).  Also: a single rank equals the plain step, and a non-finite
 gradient on one rank skips every rank's update."""
@@ -58,9 +58,9 @@ def test_device_exchange_same_bits_as_host_exchange(dev, world, n, gdt):
             if gdt == "bf16":
                 gs = [g.to(torch.bfloat16) for g in gs]
             if mode == "host":
-                total = sharded.ordered_sum(osr.grad_sumsq_typed(c, g) for c, g in zip(ctxs, gs))
+                sums = [osr.grad_sumsq_typed(c, g) for c, g in zip(ctxs, gs)]
                 for c, (_, _, (w, m, v)), g in zip(ctxs, parts, gs):
-                    osr.adamw_clip_step_mixed(c, w, g, m, v, t, LR, WD, CLIP, global_sumsq=total)
+                    osr.adamw_clip_step_ranks(c, w, g, m, v, t, LR, WD, CLIP, sums)
             else:
                 for r, (c, g) in enumerate(zip(ctxs, gs)):
                     osr.grad_sumsq_to(c, g, recv[r:r + 1])

@@ -1,7 +1,8 @@
 """Host logic of the sharded step on CPU ranks (gloo, world sizes 2 and 4):
-the partition covers [0, n) exactly, the rank-ordered exchange gives every
-rank the same global sum, and the oracle applied shard by shard with that
-sum reproduces the unsharded oracle step."""
+the partition covers [0, n) exactly, the library's rank-order sum of the
+gathered values (adamw_rank_total, host only) gives every rank the same
+global sum, and the oracle applied shard by shard with that sum reproduces
+the unsharded oracle step."""
 import os
 import socket
 
@@ -9,7 +10,8 @@ import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
-from optimizer_step_resumable_gb300.sharded import ordered_sum, shard_range
+import optimizer_step_resumable_gb300 as osr
+from optimizer_step_resumable_gb300.sharded import shard_range
 
 
 def test_shard_ranges_cover_exactly():
@@ -27,9 +29,41 @@ def test_shard_ranges_cover_exactly():
         shard_range(3, 0, 4)
 
 
-def test_ordered_sum_is_rank_order():
-    parts = [1e16, 1.0, -1e16, 1.0]
-    assert ordered_sum(parts) == ((1e16 + 1.0) - 1e16) + 1.0
+def test_rank_total_adds_in_rank_order(lib):
+    # 1 + 2^-53 rounds to 1 (ties to even), so the order of the additions
+    # shows in the last bit: rank order keeps 1, the reverse order gives
+    # 1 + 2^-52
+    tiny = 2.0 ** -53
+    assert osr.adamw_rank_total([1.0, tiny, tiny], 1.0)[0] == 1.0
+    assert osr.adamw_rank_total([tiny, tiny, 1.0], 1.0)[0] == 1.0 + 2.0 ** -52
+
+
+def test_rank_total_norm_and_factor(lib):
+    # 3-4-5: the ranks hold 9 and 16, the norm is 5 and the factor c / 5
+    s, norm, scale = osr.adamw_rank_total([9.0, 16.0], 1.0)
+    assert (s, norm) == (25.0, 5.0)
+    assert scale == float(np.float32(0.2))
+    # the gradient scale multiplies the norm and the factor applied to g
+    s, norm, scale = osr.adamw_rank_total([9.0, 16.0], 1.0, grad_scale=0.5)
+    assert norm == 2.5 and scale == float(np.float32(0.5 * (1.0 / 2.5)))
+    # at or below the threshold the factor is exactly 1 (strict >)
+    assert osr.adamw_rank_total([9.0, 16.0], 5.0)[2] == 1.0
+    assert osr.adamw_rank_total([0.0, 0.0], 1.0)[1:] == (0.0, 1.0)
+    assert osr.adamw_rank_total([9.0, 16.0], float("inf"))[2] == 1.0
+
+
+def test_rank_total_refusals(lib):
+    for bad in ([float("inf"), 1.0], [1.0, float("nan")]):
+        with pytest.raises(osr.NonFiniteGradient) as e:
+            osr.adamw_rank_total(bad, 1.0)
+        assert not np.isfinite(e.value.values[1])
+    for parts, clip, gs in (([1.0, -1.0], 1.0, 1.0), ([1.0], 0.0, 1.0), ([1.0], 1.0, 0.0),
+                            ([1.0], 1.0, float("inf"))):
+        with pytest.raises(osr.AdamWError) as e:
+            osr.adamw_rank_total(parts, clip, grad_scale=gs)
+        assert e.value.status == osr.EINVAL
+    with pytest.raises(ValueError):
+        osr.adamw_rank_total([], 1.0)
 
 
 def _free_port():
@@ -43,7 +77,8 @@ def _rank_main(rank, world, port, n, out_dir):
 
     import oracle
     import synthetic
-    from optimizer_step_resumable_gb300.sharded import global_sumsq, shard_range
+    import optimizer_step_resumable_gb300 as osr
+    from optimizer_step_resumable_gb300.sharded import gather_sumsq, shard_range
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -55,7 +90,9 @@ def _rank_main(rank, world, port, n, out_dir):
     v = np.zeros(k, np.float32)
     for t in (1, 2, 3):
         g = synthetic.grads(7, t, 1e-2, idx=idx, outlier_frac=0.01, outlier_mult=100.0)
-        total = global_sumsq(o.sumsq(g))
+        parts = gather_sumsq(o.sumsq(g))
+        assert len(parts) == world
+        total = osr.adamw_rank_total(parts, 1.0)[0]  # the library's rank-order sum
         s = o.clip_scale(np.sqrt(total), 1.0)
         w, m, v = o.adamw_at(np.arange(k), w, g, m, v, s, t, 3e-3, 0.01)
         np.save(os.path.join(out_dir, f"r{rank}_t{t}_total.npy"), np.array([total]))
@@ -65,7 +102,7 @@ def _rank_main(rank, world, port, n, out_dir):
 
 
 @pytest.mark.parametrize("world", [2, 4])
-def test_sharded_oracle_matches_unsharded(oracle, tmp_path, world):
+def test_sharded_oracle_matches_unsharded(oracle, lib, tmp_path, world):
     n = 65536 + 37
     mp.start_processes(_rank_main, args=(world, _free_port(), n, str(tmp_path)),
                        nprocs=world, join=True, start_method="spawn")
