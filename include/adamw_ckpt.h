@@ -156,9 +156,11 @@ ADAMW_API int grad_global_norm(adamw_ctx* ctx, const float* d_g, double* h_norm,
  * t >= 1 is the 1-based index of this update (t counts real optimizer
  * updates only).  clip > 0 (INFINITY disables clipping); lr, wd >= 0.
  * d_g is read only.  The bias-correction scalars are computed on the host in
- * double.  Two kernels on `stream`: the norm reduction, then the fused
- * clip-scale + AdamW pass that reads w, g, m, v once and writes w, m, v
- * once.  If the norm is not finite the second kernel leaves w, m, v
+ * double.  Two kernels on `stream`: the norm reduction's fixed per-block
+ * partial sums, then the fused clip-scale + AdamW pass, whose blocks each
+ * add up those partials in the same fixed order (the same bits in every
+ * block; block 0 records the norm) and then read w, g, m, v once and write
+ * w, m, v once.  If the norm is not finite the second kernel leaves w, m, v
  * untouched; the call itself does not wait, so that outcome is reported by
  * adamw_last_norm().  Decay applies to every parameter.
  */

@@ -126,14 +126,16 @@ int validate_table(int64_t n, const int64_t* offsets, const int64_t* numels, int
     return ADAMW_OK;
 }
 
+// tail = false: the norm kernel leaves only its partials, and the fused
+// kernel launched next finishes the reduction (osr::NormFinish).
 int launch_norm_on(adamw_ctx* c, const void* g, double clip, void* stream,
                    double grad_scale = 1.0, bool tensor_sums = false,
-                   int32_t g_dtype = ADAMW_DTYPE_F32)
+                   int32_t g_dtype = ADAMW_DTYPE_F32, bool tail = true)
 {
     const osr::TensorSegs segs{c->d_tab_offsets, c->d_kfirst, c->d_segbase, c->d_seg_sums};
     const int e = osr::launch_norm(g, c->n, clip, c->d_partials, c->d_counter, c->d_res,
                                    c->h_res_dev, stream, grad_scale,
-                                   tensor_sums ? &segs : nullptr, g_dtype);
+                                   tensor_sums ? &segs : nullptr, g_dtype, tail);
     if (e != cudaSuccess)
         return cuda_fail(cudaError_t(e), "norm kernel launch");
     c->segs_launched = tensor_sums;
@@ -219,6 +221,7 @@ StepScalars make_step_scalars(const adamw_ctx* c, int32_t t, double lr, double w
     k.scale = 1.0f;
     k.decay_mask = c->decay_mask_on ? c->d_decay_mask : nullptr;
     k.chunk_ctr = (c->dynamic_chunks && c->n >= kDynamicChunksMinN) ? c->d_chunk_ctr : nullptr;
+    k.fin = NormFinish{nullptr, 0, 0.0, 1.0, nullptr, nullptr};
     return k;
 }
 
@@ -571,10 +574,13 @@ static int step_impl(adamw_ctx* ctx, float* d_w, void* d_g, int32_t g_dtype, flo
             return cuda_fail(cudaError_t(e), "global-sum kernel launch");
         ctx->segs_launched = false;
     } else if (!external) {
+        // the norm kernel writes its partials; the fused kernel sums them
         rc = launch_norm_on(ctx, d_g, clip, stream, grad_scale,
-                            (flags & ADAMW_TENSOR_NORMS) != 0, g_dtype);
+                            (flags & ADAMW_TENSOR_NORMS) != 0, g_dtype, false);
         if (rc != ADAMW_OK)
             return rc;
+        k.fin = osr::NormFinish{ctx->d_partials, osr::norm_blocks(ctx->n), clip, grad_scale,
+                                ctx->d_res, ctx->h_res_dev};
     }
     if (prof[1])
         CUDA_TRY(cudaEventRecord(prof[1], st));

@@ -48,7 +48,9 @@ void fill_args(const adamw_ctx* c, double clip, const StepScalars& k, NormNodeAr
     aa->v = c->graph_v;
     aa->n = c->n;
     aa->k = k;
-    aa->d_res = c->d_res;
+    // the norm node leaves its partials: the fused node sums them
+    aa->k.fin = NormFinish{c->d_partials, norm_blocks(c->n), clip, 1.0, c->d_res, c->h_res_dev};
+    aa->d_res = nullptr;
     adamw_node_params(aa, c->caps, ap);
 }
 

@@ -31,6 +31,18 @@ struct NormResult {
                         // barrier wait ran out; cleared by the host
 };
 
+// The second level of a norm reduction whose kernel ran without its last
+// block (partials only): every block of the fused kernel that follows sums
+// partials[0..nparts) in the norm kernel's fixed order itself -- the same
+// bits in every block -- and block 0 publishes the result record.
+struct NormFinish {
+    const double* partials;  // NULL: not used (the factor comes from elsewhere)
+    int32_t nparts;
+    double clip, grad_scale;
+    NormResult* d_res;  // result record (device)
+    NormResult* h_res;  // its host-mapped mirror (device address), may be NULL
+};
+
 // Per-step scalars, computed on the host in double and rounded to float once.
 struct StepScalars {
     float beta1, omb1;      // beta1 and 1 - beta1
@@ -47,6 +59,8 @@ struct StepScalars {
     // hand out, [1] blocks done (both 0 between launches: the last block
     // out resets them).  NULL: chunks are dealt out cyclically by block.
     uint32_t* chunk_ctr;
+    // Finish of the norm reduction in the fused kernel (see NormFinish).
+    NormFinish fin;
 };
 
 // Tunables of the kernels (fixed at compile time; used in norm.cu, step.cu).
@@ -100,10 +114,12 @@ inline int64_t norm_block_tile(int64_t n, int b)
 // Element types of the gradient and of the optional 16-bit weight copy.
 constexpr int32_t kDtypeF32 = 0, kDtypeBF16 = 1, kDtypeF16 = 2;
 
+// tail = false: the kernel only writes its P partials (no ticket, no last
+// block); the fused kernel launched next finishes the reduction (NormFinish).
 int launch_norm(const void* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
                 void* stream, double grad_scale = 1.0, const TensorSegs* segs = nullptr,
-                int32_t g_dtype = kDtypeF32);
+                int32_t g_dtype = kDtypeF32, bool tail = true);
 // g of type g_dtype (16-byte aligned for float32 on the vector path, 8-byte
 // for 16-bit types); w_lp (may be NULL) receives the new weights rounded to
 // w_lp_dtype (bfloat16 or binary16; 8-byte aligned).  16-bit types and the
@@ -155,6 +171,8 @@ int launch_pack(const float* w, const float* m, const float* v, int64_t n, int32
 
 // Kernel-node parameters for a CUDA graph of one step (graph.cu).  The
 // argument structs own the values that kernelParams point into.
+// (The step graph's norm node runs without its last block: the fused node
+// finishes the reduction.)
 struct NormNodeArgs {
     const float* g;
     int64_t n;

@@ -127,7 +127,7 @@ extern "C" int adamw_clip_step_noalloc(float* d_w, const float* d_g, float* d_m,
 
     const double bc1 = 1.0 - std::pow(beta1, double(t));
     const double bc2 = 1.0 - std::pow(beta2, double(t));
-    osr::StepScalars k;
+    osr::StepScalars k{};  // (k.fin unused: the norm kernel publishes its result)
     k.beta1 = float(beta1);
     k.omb1 = float(1.0 - beta1);
     k.beta2 = float(beta2);

@@ -39,6 +39,14 @@ using normdev::thread_sumsq_in;
 // root and the clip factor, and publishes the result.  No block waits on
 // another; the ticket counter is reset for the next launch.
 //
+// kTail = false: no ticket and no last block -- each block writes its
+// partial and leaves.  The fused kernel launched right after (a programmatic
+// dependent, or plain stream order) then sums the partials itself, in the
+// same order, once per block (NormFinish): the step's result is the same
+// bits, and the serial tail -- fence, ticket atomic, fence, reads of the
+// partials, result stores, about 3 us on GB300 at every size -- is no longer
+// between the two kernels.
+//
 // kSegs: also the sum of squares of each tensor of the offset table, at no
 // extra traffic.  Because a block's tiles are contiguous, its threads keep
 // one running sum for the tensor they are in; on a tile where a tensor
@@ -50,7 +58,7 @@ using normdev::thread_sumsq_in;
 // ---------------------------------------------------------------------------
 // (at least 4 resident blocks per SM, so that the fixed 608-block grid is one
 // wave on 152 SMs whichever variant runs)
-template <bool kVec, bool kSegs, typename G>
+template <bool kVec, bool kSegs, typename G, bool kTail>
 __global__ void __launch_bounds__(kNormThreads, 4)
     k_grad_norm(const G* __restrict__ g, int64_t n, double clip, double grad_scale,
                 double* __restrict__ partials, unsigned int* __restrict__ counter,
@@ -112,6 +120,11 @@ __global__ void __launch_bounds__(kNormThreads, 4)
     }
 
     acc = block_sum<kNormThreads>(acc);
+    if constexpr (!kTail) {
+        if (tid == 0)
+            partials[blockIdx.x] = acc;
+        return;
+    }
     __shared__ bool is_last;
     if (tid == 0) {
         partials[blockIdx.x] = acc;
@@ -135,45 +148,59 @@ __global__ void __launch_bounds__(kNormThreads, 4)
 
 namespace {
 
-template <typename G, bool kVec>
-void launch_norm_typed(const void* g, int64_t n, double clip, double* partials,
-                       unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                       cudaStream_t s, double grad_scale, const TensorSegs* segs)
+template <typename G, bool kVec, bool kTail>
+void launch_norm_tail(const void* g, int64_t n, double clip, double* partials,
+                      unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                      cudaStream_t s, double grad_scale, const TensorSegs* segs)
 {
     const int blocks = norm_blocks(n);
     const TensorSegs none{nullptr, nullptr, nullptr, nullptr};
     const G* gt = static_cast<const G*>(g);
     if (segs)
-        k_grad_norm<kVec, true, G><<<blocks, kNormThreads, 0, s>>>(
+        k_grad_norm<kVec, true, G, kTail><<<blocks, kNormThreads, 0, s>>>(
             gt, n, clip, grad_scale, partials, counter, d_res, h_res_dev, *segs);
     else
-        k_grad_norm<kVec, false, G><<<blocks, kNormThreads, 0, s>>>(
+        k_grad_norm<kVec, false, G, kTail><<<blocks, kNormThreads, 0, s>>>(
             gt, n, clip, grad_scale, partials, counter, d_res, h_res_dev, none);
+}
+
+template <typename G, bool kVec>
+void launch_norm_typed(const void* g, int64_t n, double clip, double* partials,
+                       unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
+                       cudaStream_t s, double grad_scale, const TensorSegs* segs, bool tail)
+{
+    if (tail)
+        launch_norm_tail<G, kVec, true>(g, n, clip, partials, counter, d_res, h_res_dev, s,
+                                        grad_scale, segs);
+    else
+        launch_norm_tail<G, kVec, false>(g, n, clip, partials, counter, d_res, h_res_dev, s,
+                                         grad_scale, segs);
 }
 
 }  // namespace
 
 int launch_norm(const void* g, int64_t n, double clip, double* partials,
                 unsigned int* counter, NormResult* d_res, NormResult* h_res_dev,
-                void* stream, double grad_scale, const TensorSegs* segs, int32_t g_dtype)
+                void* stream, double grad_scale, const TensorSegs* segs, int32_t g_dtype,
+                bool tail)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (g_dtype) {
     case kDtypeBF16:  // 8-byte alignment checked by the caller
         launch_norm_typed<__nv_bfloat16, true>(g, n, clip, partials, counter, d_res, h_res_dev,
-                                               s, grad_scale, segs);
+                                               s, grad_scale, segs, tail);
         break;
     case kDtypeF16:
         launch_norm_typed<__half, true>(g, n, clip, partials, counter, d_res, h_res_dev, s,
-                                        grad_scale, segs);
+                                        grad_scale, segs, tail);
         break;
     default:
         if (detail::aligned16(g))
             launch_norm_typed<float, true>(g, n, clip, partials, counter, d_res, h_res_dev, s,
-                                           grad_scale, segs);
+                                           grad_scale, segs, tail);
         else
             launch_norm_typed<float, false>(g, n, clip, partials, counter, d_res, h_res_dev, s,
-                                            grad_scale, segs);
+                                            grad_scale, segs, tail);
     }
     return int(cudaGetLastError());
 }
@@ -190,8 +217,10 @@ int norm_node_params(NormNodeArgs* a, cudaKernelNodeParams* p)
     a->ptrs[7] = &a->h_res;
     a->segs = TensorSegs{nullptr, nullptr, nullptr, nullptr};
     a->ptrs[8] = &a->segs;
-    p->func = detail::aligned16(a->g) ? reinterpret_cast<void*>(&k_grad_norm<true, false, float>)
-                                      : reinterpret_cast<void*>(&k_grad_norm<false, false, float>);
+    // without the last block: the fused node finishes the reduction
+    p->func = detail::aligned16(a->g)
+                  ? reinterpret_cast<void*>(&k_grad_norm<true, false, float, false>)
+                  : reinterpret_cast<void*>(&k_grad_norm<false, false, float, false>);
     p->gridDim = dim3(unsigned(norm_blocks(a->n)));
     p->blockDim = dim3(kNormThreads);
     p->sharedMemBytes = 0;

@@ -18,6 +18,7 @@
 #include "adamw_dev.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "norm_dev.cuh"
 
 namespace osr {
 namespace {
@@ -37,6 +38,10 @@ using adamwdev::kStepVec;
 // not void, is the type of a 16-bit copy of the new weights written to w_lp
 // (rounded to nearest even) for the next forward pass.  kMask: k.decay_mask
 // holds one decay flag per element, as decay_nibble reads it.
+// With k.fin.partials set, the norm kernel before this one left only its
+// per-block partial sums: every block adds them up here in the norm kernel's
+// fixed order (normdev::sum_partials, the same bits in every block), takes
+// the factor from the total, and block 0 publishes the result record.
 // (at least 4 resident blocks per SM, the occupancy the launch is sized for,
 // whichever variant runs)
 template <bool kVec, bool kZero, typename G, typename WL, bool kMask>
@@ -51,7 +56,8 @@ __global__ void __launch_bounds__(kStepThreads, 4)
     // L2 with this block's first chunk (inputs the norm kernel does not
     // write), then wait for the norm grid to finish before reading its
     // result.  Launched normally, the wait returns at once.
-    if (kVec && res) {
+    static_assert(kStepThreads == kNormThreads, "the block sums the norm partials");
+    if (kVec && (res || k.fin.partials)) {
         const int64_t i0 = int64_t(blockIdx.x) * kStepThreads * kStepVec + threadIdx.x;
         if ((i0 + (kStepVec - 1) * kStepThreads) < (n >> 2)) {
 #pragma unroll
@@ -66,7 +72,24 @@ __global__ void __launch_bounds__(kStepThreads, 4)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     float s = k.scale;
-    if (res) {
+    if (k.fin.partials) {
+        __shared__ float s_scale;
+        __shared__ int s_skip;
+        const double total = normdev::sum_partials(k.fin.partials, k.fin.nparts);
+        if (threadIdx.x == 0) {
+            // only block 0 publishes, so only it reads the record's sequence number
+            const NormResult r = normdev::make_result(
+                total, k.fin.clip, k.fin.grad_scale, blockIdx.x == 0 ? k.fin.d_res->seq + 1u : 0u);
+            s_scale = r.scale;
+            s_skip = r.nonfinite;
+            if (blockIdx.x == 0)
+                normdev::publish(r, k.fin.d_res, k.fin.h_res);
+        }
+        __syncthreads();
+        if (s_skip)
+            return;
+        s = s_scale;
+    } else if (res) {
         if (res->nonfinite)
             return;
         s = res->scale;
