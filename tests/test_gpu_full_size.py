@@ -1,0 +1,128 @@
+"""Every element of one full-size step against the oracle.
+
+The 110M tensor list (196 tensors, n = 110,418,432; the fused kernel hands
+its chunks out by a counter at this size), one step at t = 7 from
+generator-made non-zero moments, so that both bias corrections and both
+moment terms are in play:
+
+* float32 gradient, decay on every parameter;
+* decay flags exempting every 1-D tensor (biases, LayerNorm gains and
+  shifts): the oracle's per-element definition with wd = 0 on those tensors;
+* bfloat16 gradient (widened exactly on both sides) with a bfloat16 copy of
+  the new weights, which must be the nearest-even rounding of the GPU's own
+  float32 weights.
+
+The oracle evaluates its per-element definition ("Training as a Recoverable
+State Transition", section "The Exact Targets of Clipping and AdamW") over
+index chunks on all host cores; its clip factor comes from its own norm of
+the whole gradient.  Bars: the norm within 1e-6 relative, w, m, v within
+1e-6 of their term magnitudes (tests/parity.py)."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+
+import synthetic
+from synthetic import device as synth_dev
+from synthetic import workloads as W
+from parity import FLOOR, RTOL_NORM, RTOL_ONE_STEP, magnitudes
+
+torch = pytest.importorskip("torch")
+import optimizer_step_resumable_gb300 as osr  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+T = 7
+CHUNK = 1 << 21
+
+
+@pytest.fixture(scope="module")
+def dev(lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def _state(dev, n):
+    """w, g (step T), m, v on the device from the input generator."""
+    w = torch.empty(n, device=dev)
+    g = torch.empty(n, device=dev)
+    m = torch.empty(n, device=dev)
+    v = torch.empty(n, device=dev)
+    synth_dev.fill_weights(w, 7)
+    synth_dev.fill_grads(g, 7, T, 1e-3)
+    synth_dev.fill(m, 7, 11, 0, 1e-3)
+    synth_dev.fill(v, 7, 12, 0, 1e-5)
+    v.abs_()
+    return w, g, m, v
+
+
+def _chunks(offsets, numels, wd, flags=None):
+    """(lo, hi, wd of the range) over the table, no range longer than CHUNK."""
+    out = []
+    for k, (off, num) in enumerate(zip(offsets, numels)):
+        wk = wd if flags is None or flags[k] else 0.0
+        for lo in range(off, off + num, CHUNK):
+            out.append((lo, min(lo + CHUNK, off + num), wk))
+    return out
+
+
+def _check_all(oracle, got, hw, hg, hm, hv, s, lr, chunks, label):
+    """Every element of got = (w, m, v) against the oracle's step."""
+
+    def one(c):
+        lo, hi, wk = c
+        idx = np.arange(lo, hi, dtype=np.int64)
+        terms = oracle.adamw_terms_at(idx, hw, hg, hm, hv, s, T, lr, wk)
+        want = oracle.adamw_at(idx, hw, hg, hm, hv, s, T, lr, wk)
+        bad = []
+        for name, a, o, mag in zip("wmv", got, want, magnitudes(terms, lr, T)):
+            err = np.abs(a[lo:hi].astype(np.float64) - o.astype(np.float64))
+            over = np.nonzero(~(err <= RTOL_ONE_STEP * mag + FLOOR))[0]
+            if over.size:
+                i = over[np.argmax(err[over] / (RTOL_ONE_STEP * mag[over] + FLOOR))]
+                bad.append(f"{name}: {over.size} elements, worst {lo + i}: got {a[lo + i]!r} "
+                           f"want {o[i]!r} magnitude {mag[i]:.3e}")
+        return bad
+
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        bad = [b for r in ex.map(one, chunks) for b in r]
+    assert not bad, f"{label}: " + "; ".join(bad[:6])
+
+
+def _run(dev, oracle, mode):
+    wl = W.gpt_110m()
+    n = wl.n
+    off, num = wl.table()
+    w, g, m, v = _state(dev, n)
+    hw, hg, hm, hv = (x.cpu().numpy() for x in (w, g, m, v))
+    flags = W.decay_flags_matrices_only(wl.tensors) if mode == "decay_flags" else None
+    w_lp = None
+    with osr.adamw_create(n, off, num, flags=osr.CREATE_NO_CKPT) as ctx:
+        if flags is not None:
+            osr.adamw_set_decay_mask(ctx, flags)
+        if mode == "bf16":
+            bits = synthetic.to_bf16_bits(hg)
+            hg = (bits.astype(np.uint32) << 16).view(np.float32)  # exact widening
+            g16 = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+            w_lp = torch.empty(n, dtype=torch.bfloat16, device=dev)
+            osr.adamw_clip_step_mixed(ctx, w, g16, m, v, T, wl.lr, wl.wd, wl.clip, w_lp=w_lp)
+        else:
+            osr.adamw_clip_step(ctx, w, g, m, v, T, wl.lr, wl.wd, wl.clip)
+        norm, _ = osr.adamw_last_norm(ctx)
+    onorm = oracle.global_norm(hg)
+    assert abs(norm - onorm) <= RTOL_NORM * onorm, (norm, onorm)
+    s = oracle.clip_scale(onorm, wl.clip)
+    assert s < 1.0  # the clip is active on this workload
+    got = [x.cpu().numpy() for x in (w, m, v)]
+    _check_all(oracle, got, hw, hg, hm, hv, s, wl.lr, _chunks(off, num, wl.wd, flags),
+               f"110M list, {mode}")
+    if w_lp is not None:
+        lp = w_lp.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(lp, synthetic.to_bf16_bits(got[0]))
+
+
+@pytest.mark.parametrize("mode", ["f32", "decay_flags", "bf16"])
+def test_gpt_110m_one_step_every_element(dev, oracle, mode):
+    _run(dev, oracle, mode)
+    torch.cuda.empty_cache()
