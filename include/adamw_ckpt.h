@@ -440,7 +440,10 @@ ADAMW_API int ckpt_pack(adamw_ctx* ctx, int32_t step, const float* d_w,
  * After the rename, rotation (if set) deletes all but the newest `keep`
  * step_*.bin files of dir.  The final path is copied to path_out (may be
  * NULL) if it fits in path_cap bytes.  ADAMW_ESTATE if there is no packed
- * image; ADAMW_EIO on any file error (the .tmp file is removed).
+ * image; ADAMW_EIO on any file error (the .tmp file is removed), and also
+ * when the fsync of dir after the rename fails (the file is then in place
+ * but the rename may not be durable; a file system that does not sync
+ * directories is not an error).
  *
  * ckpt_write blocks the calling thread until the file is durable.
  * ckpt_write_async hands the same work to the context's writer thread and
@@ -530,7 +533,10 @@ ADAMW_API int ckpt_read(adamw_ctx* ctx, const char* path, int32_t* step_out,
  * any n in [1, 2^31 - 1] (the reduction grid is capped); n outside that range
  * is rejected with ADAMW_EINVAL.  The first call on each device resolves
  * that array's address and the kernels' launch limits (no allocation); make
- * that first call before any stream capture.  All calls share the one array
+ * that first call before any stream capture.  Those values are kept for the
+ * life of the process: after a cudaDeviceReset (which unloads the library's
+ * device code and its array) the kept address is stale, so a caller that
+ * resets a device must not call this entry point on it again.  All calls share the one array
  * and it keeps the last call's contents (each call clears the part that must
  * start at zero): calls that overlap on the GPU -- on different streams or
  * from different threads without ordering -- race and give wrong results.

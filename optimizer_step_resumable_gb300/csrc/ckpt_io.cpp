@@ -79,6 +79,24 @@ int write_exact(int fd, const void* src, size_t bytes, const char* path, int* er
     }
     return ADAMW_OK;
 }
+// fsync of the directory that holds a file just renamed, so that the rename
+// itself is on disk.  A directory that cannot be opened read-only, or a file
+// system that does not sync directories (fsync: EINVAL, ENOTSUP, EROFS), is
+// tolerated; any other failure (EIO, ENOSPC, ...) means the rename may not be
+// durable and is reported as ADAMW_EIO.
+int sync_dir(const char* dir)
+{
+    const int dfd = ::open(dir, O_RDONLY | O_DIRECTORY | O_CLOEXEC);
+    if (dfd < 0)
+        return ADAMW_OK;
+    int rc = ADAMW_OK;
+    if (::fsync(dfd) != 0 && errno != EINVAL && errno != ENOTSUP && errno != EROFS)
+        rc = fail(ADAMW_EIO, "fsync of directory %s: %s (the rename may not be durable)", dir,
+                  std::strerror(errno));
+    ::close(dfd);
+    return rc;
+}
+
 }  // namespace
 
 int fail(int status, const char* fmt, ...)
@@ -186,11 +204,8 @@ int write_named_file(const char* dir, const char* name, const IoPiece* pieces, i
         ::unlink(tmp_path);
         return rc;
     }
-    const int dfd = ::open(dir, O_RDONLY | O_CLOEXEC);
-    if (dfd >= 0) {
-        ::fsync(dfd);
-        ::close(dfd);
-    }
+    if ((rc = sync_dir(dir)) != ADAMW_OK)
+        return rc;
     if (path_out && path_cap > 0) {
         if (size_t(len) + 1 > path_cap)
             return fail(ADAMW_EINVAL, "ckpt write: path buffer too small (file written)");
@@ -308,11 +323,8 @@ int AtomicFile::commit(char* path_out, size_t path_cap)
         ::unlink(tmp_.c_str());
         return rc;
     }
-    const int dfd = ::open(dir_.c_str(), O_RDONLY | O_CLOEXEC);
-    if (dfd >= 0) {
-        ::fsync(dfd);
-        ::close(dfd);
-    }
+    if ((rc = sync_dir(dir_.c_str())) != ADAMW_OK)
+        return rc;
     if (path_out && path_cap > 0) {
         if (final_.size() + 1 > path_cap)
             return fail(ADAMW_EINVAL, "ckpt write: path buffer too small (file written)");
