@@ -1,8 +1,8 @@
-"""The README's Python example runs as written (sizes shrunk, checkpoint
-directory moved into a temporary one), so the documented calls stay the
-library's calls."""
+"""The quick-start example (examples/quickstart.py) runs as written, at a
+small size with its checkpoints in a temporary directory, so the documented
+calls stay the library's calls."""
+import importlib.util
 import os
-import re
 
 import pytest
 
@@ -13,16 +13,14 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_readme_python_example_runs(lib, tmp_path):
+def test_quickstart_example_runs(lib, tmp_path):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-    text = open(os.path.join(ROOT, "README.md")).read()
-    code = re.search(r"```python\n(.*?)```", text, re.S).group(1)
-    for big, small in (("110_418_432", "65_600"), ("24_576_000", "30_000")):
-        assert big in code
-        code = code.replace(big, small)
-    code = code.replace('"ckpt/', repr(str(tmp_path)).strip("'\"").join(['"', '/']))
-    scope = {}
-    exec(compile(code, "README.md", "exec"), scope)
-    assert os.path.exists(tmp_path / "step_000200.bin")
-    assert osr.ckpt_probe(str(tmp_path / "step_000200.bin")) == (200, 65_600)
-    assert scope["step"] == 200
+    spec = importlib.util.spec_from_file_location(
+        "quickstart", os.path.join(ROOT, "examples", "quickstart.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    step, norm, factor = mod.main(n=65_600, first=30_000, directory=str(tmp_path))
+    assert step == 200 and norm > 0 and 0 < factor <= 1
+    path = tmp_path / "step_000200.bin"
+    assert osr.ckpt_probe(str(path)) == (200, 65_600)
+    assert os.path.exists(tmp_path / "step_000100.bin")
