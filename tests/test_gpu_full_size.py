@@ -1,9 +1,9 @@
 """Every element of one full-size step against the oracle.
 
 The 110M tensor list (196 tensors, n = 110,418,432; the fused kernel hands
-its chunks out by a counter at this size), one step at t = 7 from
-generator-made non-zero moments, so that both bias corrections and both
-moment terms are in play:
+its chunks out by a counter at this size) and the flat 2^30-parameter (1B)
+state, one step at t = 7 from generator-made non-zero moments, so that both
+bias corrections and both moment terms are in play.  On the 110M list:
 
 * float32 gradient, decay on every parameter;
 * decay flags exempting every 1-D tensor (biases, LayerNorm gains and
@@ -43,14 +43,14 @@ def dev(lib):
     return torch.device("cuda:0")
 
 
-def _state(dev, n):
+def _state(dev, n, outlier_frac=0.0, outlier_mult=1.0):
     """w, g (step T), m, v on the device from the input generator."""
     w = torch.empty(n, device=dev)
     g = torch.empty(n, device=dev)
     m = torch.empty(n, device=dev)
     v = torch.empty(n, device=dev)
     synth_dev.fill_weights(w, 7)
-    synth_dev.fill_grads(g, 7, T, 1e-3)
+    synth_dev.fill_grads(g, 7, T, 1e-3, outlier_frac, outlier_mult)
     synth_dev.fill(m, 7, 11, 0, 1e-3)
     synth_dev.fill(v, 7, 12, 0, 1e-5)
     v.abs_()
@@ -126,3 +126,36 @@ def _run(dev, oracle, mode):
 def test_gpt_110m_one_step_every_element(dev, oracle, mode):
     _run(dev, oracle, mode)
     torch.cuda.empty_cache()
+
+
+def _host_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def test_flat_1b_one_step_every_element(dev, oracle):
+    """The 1B configuration (flat 2^30, g ~ 1e-3 with 0.1% outliers x1000):
+    all 1,073,741,824 elements of w, m and v against the oracle."""
+    wl = W.flat_pow2(30)
+    n = wl.n
+    if _host_available_bytes() < (48 << 30):
+        pytest.skip("needs about 40 GB of host memory for the host copies and the oracle")
+    w, g, m, v = _state(dev, n, wl.outlier_frac, wl.outlier_mult)
+    hw, hg, hm, hv = (x.cpu().numpy() for x in (w, g, m, v))
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+        osr.adamw_clip_step(ctx, w, g, m, v, T, wl.lr, wl.wd, wl.clip)
+        norm, _ = osr.adamw_last_norm(ctx)
+    onorm = oracle.global_norm(hg)
+    assert abs(norm - onorm) <= RTOL_NORM * onorm, (norm, onorm)
+    s = oracle.clip_scale(onorm, wl.clip)
+    assert s < 1.0
+    got = [x.cpu().numpy() for x in (w, m, v)]
+    del w, g, m, v
+    torch.cuda.empty_cache()
+    _check_all(oracle, got, hw, hg, hm, hv, s, wl.lr, _chunks([0], [n], wl.wd), "flat 2^30")
