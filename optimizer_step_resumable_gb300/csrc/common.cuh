@@ -70,6 +70,36 @@ __device__ __forceinline__ float4 load4_cs<__half>(const __half* p)
                        __half2float(__ushort_as_half(static_cast<unsigned short>(r.y >> 16))));
 }
 
+// 4 elements with the default L2 caching (ld.global.cg): for data that a
+// following kernel reads again (the norm's read of g, which the fused kernel
+// reads next), so that it may still find it in L2
+template <typename G>
+__device__ __forceinline__ float4 load4_cg(const G* p);
+
+template <>
+__device__ __forceinline__ float4 load4_cg<float>(const float* p)
+{
+    return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+template <>
+__device__ __forceinline__ float4 load4_cg<__nv_bfloat16>(const __nv_bfloat16* p)
+{
+    const uint2 r = __ldcg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                       __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+}
+
+template <>
+__device__ __forceinline__ float4 load4_cg<__half>(const __half* p)
+{
+    const uint2 r = __ldcg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__half2float(__ushort_as_half(static_cast<unsigned short>(r.x & 0xffffu))),
+                       __half2float(__ushort_as_half(static_cast<unsigned short>(r.x >> 16))),
+                       __half2float(__ushort_as_half(static_cast<unsigned short>(r.y & 0xffffu))),
+                       __half2float(__ushort_as_half(static_cast<unsigned short>(r.y >> 16))));
+}
+
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const __half* p) { return __half2float(*p); }
