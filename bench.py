@@ -577,16 +577,16 @@ def run_ours(args):
         if ev is not None:
             ev[2].record(main)
 
+    # (1) the timed region of `value`: K steps as the library runs them, right
+    # after the W warm-up steps (no idle gap between them, so the first timed
+    # steps do not start on a GPU that has been idle)
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if sampler.proc else 0)
+    barrier(world)
     t = 1
     for _ in range(W):
         step(t)
         t += 1
-    torch.cuda.synchronize()
-
-    # (1) the timed region of `value`: K steps as the library runs them
-    sampler = ClockSampler(local, enabled=not args.no_clocks)
-    time.sleep(0.3 if sampler.proc else 0)
-    barrier(world)
     elapsed_ms, _ = time_region(step, t, K, main)
     t += K
     barrier(world)
