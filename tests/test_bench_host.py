@@ -73,3 +73,17 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_kernel_stats_rates_and_fractions():
+    # two steps of n = 1e6 parameters: norm 0.001 ms and 0.003 ms (mean 0.002),
+    # fused 0.01 ms each; 4 and 28 algorithmic bytes per parameter
+    n = 1_000_000
+    ks = bench.kernel_stats([(0.001, 0.01), (0.003, 0.01)], n, peak=2000.0)
+    assert ks["k_grad_norm"]["avg_ms"] == pytest.approx(0.002)
+    assert ks["k_grad_norm"]["min_ms"] == pytest.approx(0.001)
+    assert ks["k_grad_norm"]["GB/s"] == pytest.approx(4 * n / 0.002 / 1e6)   # 2000 GB/s
+    assert ks["k_grad_norm"]["frac"] == pytest.approx(1.0)
+    assert ks["k_clip_adamw"]["GB/s"] == pytest.approx(28 * n / 0.01 / 1e6)  # 2800 GB/s
+    assert ks["k_clip_adamw"]["frac"] == pytest.approx(1.4)
+    assert ks["k_clip_adamw"]["frac_of_nominal_8tbs"] == pytest.approx(2800 / 8000)
