@@ -297,9 +297,9 @@ ADAMW_API int adamw_clip_step_ranks(adamw_ctx* ctx, float* d_w, void* d_g, int32
  * One step as a CUDA graph, for states small enough that launch latency
  * dominates (e.g. 65,536 parameters: L2-resident, a few microseconds per
  * kernel).  adamw_graph_create builds, for these buffers, a graph of the norm
- * kernel followed by the fused clip+AdamW kernel -- or, where adamw_clip_step
- * would take the one-launch step (see adamw_set_launch_options), that step
- * as one kernel node (a cluster or a cooperative grid, as there) -- with
+ * kernel followed by the fused clip+AdamW kernel -- or, up to 65,536
+ * parameters, the one-launch step in its cluster form as one kernel node
+ * (see adamw_set_launch_options) -- with
  * the same results bit for bit as
  * adamw_clip_step, and instantiates it; the context owns it (replaced by the
  * next adamw_graph_create, freed by adamw_graph_destroy or adamw_destroy).
@@ -378,9 +378,11 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * instrumentation event between the kernels also implies plain order.)
  * States of up to 2^19 parameters (float32 gradient, 16-byte aligned arrays,
  * no weight copy, no per-tensor norms, no global_sumsq) take the whole step
- * as one launch instead (one kernel node when the stream is being
- * captured): the same partial sums, the same fixed-order total and the same
- * update, so the same bits, at half the launch cost.  Up to 65,536
+ * as one launch instead: the same partial sums, the same fixed-order total
+ * and the same update, so the same bits, at half the launch cost.  When the
+ * stream is being captured into a graph (no launch cost to save), only the
+ * cluster form below is used as one kernel node; larger captured steps are
+ * two kernel nodes, which take less GPU time there.  Up to 65,536
  * parameters (without ADAMW_ZERO_GRAD) the launch is thread-block clusters
  * of 8 CTAs, each cluster computing the norm itself and meeting at its
  * hardware barrier; otherwise a cooperative grid whose blocks meet at a
@@ -394,10 +396,11 @@ ADAMW_API int adamw_last_norm(adamw_ctx* ctx, double* norm_out, float* scale_out
  * end; the results are the same bits.  ADAMW_LAUNCH_STATIC_CHUNKS deals
  * chunks out cyclically by block at every size.
  * ADAMW_LAUNCH_TEST_BARRIER_TIMEOUT (for tests of that path): the next
- * one-launch step runs as the cooperative grid at any one-launch size (in a
- * step graph: above 65,536 parameters, where the node is that grid) and
- * waits for one block more than it launched, so its barrier runs out after
- * about a second, as above.  Used once, then cleared.
+ * one-launch step runs as the cooperative grid at any one-launch size (a
+ * captured step too; in a step graph above 65,536 parameters, whose next
+ * step rebuilds the graph with that grid as its node) and waits for one
+ * block more than it launched, so its barrier runs out after about a
+ * second, as above.  Used once, then cleared.
  */
 ADAMW_API int adamw_set_launch_options(adamw_ctx* ctx, int32_t flags);
 

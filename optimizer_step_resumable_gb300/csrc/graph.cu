@@ -63,9 +63,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Whether the graph takes the one-launch step (the same rule as
 // adamw_clip_step's).
+// The one-launch node only in its cluster form (up to 65,536 parameters):
+// in a graph, with no launch overhead to save, the two-node step costs less
+// GPU time than the cooperative grid above that size.  The barrier-timeout
+// test flag asks for the grid (its next graph step rebuilds the graph).
 bool want_onepass(const adamw_ctx* c)
 {
     return c->onepass && c->n <= c->onepass_max_n &&
+           (onepass_is_cluster(c->n) || c->onepass_fault_test) &&
            onepass_grid(c->n, c->onepass_capacity) <= c->onepass_capacity &&
            aligned16(c->graph_w) && aligned16(c->graph_g) && aligned16(c->graph_m) &&
            aligned16(c->graph_v);

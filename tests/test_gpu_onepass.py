@@ -119,10 +119,12 @@ def test_large_or_unaligned_states_take_two_launches(dev):
             osr.adamw_last_norm(ctx)
 
 
-def test_captured_one_launch_steps_match_eager_two_launch_steps(dev):
-    """Steps captured into a graph (cooperative kernel nodes) replay to the
-    bits of eager two-launch steps."""
-    n = 65_573
+@pytest.mark.parametrize("n", [40_003, 65_573])
+def test_captured_steps_match_eager_two_launch_steps(dev, n):
+    """Steps captured into a graph replay to the bits of eager two-launch
+    steps: at 40,003 parameters each step is one cluster-kernel node; at
+    65,573 (above the cluster form) captured steps are two kernel nodes,
+    which take less GPU time there than the cooperative grid."""
     hw, hm, hv = inputs(n)
     hg = synthetic.grads(7, 1, 1e-2, n=n, outlier_frac=0.01, outlier_mult=100.0)
     a = [torch.from_numpy(x).to(dev) for x in (hw, hg, hm, hv)]
@@ -150,11 +152,11 @@ def test_captured_one_launch_steps_match_eager_two_launch_steps(dev):
 
 
 def test_step_graph_one_node_matches_plain_steps(dev):
-    """The library's step graph at a one-launch size is one cooperative node;
+    """The library's step graph up to 65,536 parameters is one cluster node;
     through a sequence that sets decay flags, switches the one-launch step
     off and on again (each change rebuilds the graph), its steps equal plain
     two-launch steps bit for bit."""
-    sizes = [1000, 3, 60_000, 5, 4_536]
+    sizes = [1000, 3, 59_992, 5, 4_536]
     num = np.array(sizes, np.int64)
     off = np.concatenate([[0], np.cumsum(num)[:-1]]).astype(np.int64)
     n = int(num.sum())
@@ -191,7 +193,10 @@ def test_step_graph_one_node_matches_plain_steps(dev):
 
 
 def test_step_graph_barrier_timeout_is_reported(dev):
-    n = 100_003  # a cooperative-grid node (up to 65,536 the node is a cluster: no timeout)
+    """Above 65,536 parameters the step graph has two nodes; the test flag
+    makes its next step rebuild it around the cooperative grid, whose
+    barrier then runs out, and the step after that rebuilds the two nodes."""
+    n = 100_003
     hw, hm, hv = inputs(n)
     w, m, v = (torch.from_numpy(x).to(dev) for x in (hw, hm, hv))
     g = torch.from_numpy(synthetic.grads(7, 1, 1e-2, n=n)).to(dev)
