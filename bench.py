@@ -76,7 +76,8 @@ def parse_args(argv=None):
                    help="per-size kernel measurements (flat 2^20..2^30, latency at 65,536); "
                         "prints one JSON object per size instead of the bench line")
     p.add_argument("--sweep-parts", default="sizes,mixed,latency",
-                   help="with --sweep: which parts to run (comma list of sizes, mixed, latency)")
+                   help="with --sweep: which parts to run (comma list of sizes, mixed, latency; "
+                        "latency includes the one-launch crossover at 2^16 .. 2^20)")
     return p.parse_args(argv)
 
 
@@ -974,9 +975,9 @@ def sweep_latency(dev, main):
     with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
         osr.adamw_graph_create(ctx, w, g, m, v)
         out = {}
-        # host-driven loops: the default step (one cooperative launch at this
-        # size), the two-launch step, the library's step graph (one
-        # cooperative node at this size, or the two-node graph)
+        # host-driven loops: the default step (one launch of thread-block
+        # clusters at this size), the two-launch step, the library's step
+        # graph (one cluster-kernel node at this size, or the two-node graph)
         for mode in ("plain", "plain_two_launch", "graph", "graph_two_node"):
             osr.adamw_set_launch_options(ctx, osr.LAUNCH_NO_ONEPASS
                                          if mode.endswith("two_launch") or
@@ -1017,7 +1018,59 @@ def sweep_latency(dev, main):
         osr.adamw_set_launch_options(ctx, 0)
     row = {"workload": wl.name, "n": n, "latency": out}
     print(json.dumps(row), flush=True)
+    del w, g, m, v
+    sweep_one_launch_crossover(dev, main)
     return 0
+
+
+def sweep_one_launch_crossover(dev, main):
+    """The library's default step against two launches at 2^16 .. 2^20
+    parameters: microseconds per host-driven step (2000 steps) and GPU time
+    per step of 50 steps captured in one graph (replayed 20 times)."""
+    import torch
+
+    import optimizer_step_resumable_gb300 as osr
+    from synthetic import device as synth_dev
+    from synthetic import workloads as W
+    for log2n in range(16, 21):
+        wl = W.flat_pow2(log2n)
+        n = wl.n
+        w = torch.empty(n, device=dev)
+        g = torch.empty(n, device=dev)
+        m = torch.zeros(n, device=dev)
+        v = torch.zeros(n, device=dev)
+        synth_dev.fill_weights(w, wl.seed)
+        synth_dev.fill_grads(g, wl.seed, 1, wl.grad_sigma, wl.outlier_frac, wl.outlier_mult)
+        row = {"workload": wl.name, "n": n}
+        with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx:
+            for mode, flags in (("default", 0), ("two_launch", osr.LAUNCH_NO_ONEPASS)):
+                osr.adamw_set_launch_options(ctx, flags)
+                for t in range(1, 20):
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                for t in range(20, 2020):
+                    osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+                b.record(main)
+                b.synchronize()
+                host_us = 1e3 * a.elapsed_time(b) / 2000
+                gr = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream()
+                with torch.cuda.stream(cap):
+                    with torch.cuda.graph(gr, stream=cap):
+                        for _ in range(50):
+                            osr.adamw_clip_step(ctx, w, g, m, v, 100, wl.lr, wl.wd, wl.clip,
+                                                stream=cap)
+                gr.replay()
+                torch.cuda.synchronize()
+                ms, _, _ = median_ms(gr.replay, 20, main)
+                row[mode] = {"host_us_per_step": host_us, "gpu_us_per_step_captured": 1e3 * ms / 50}
+                del gr
+            osr.adamw_set_launch_options(ctx, 0)
+        print(json.dumps(row), flush=True)
+        del w, g, m, v
+        torch.cuda.empty_cache()
 
 
 def main(argv=None):

@@ -105,7 +105,7 @@ struct adamw_ctx {
     float* graph_m = nullptr;
     float* graph_v = nullptr;
     bool graph_mask = false;  // the graph's fused node reads decay flags
-    bool graph_onepass = false;  // one cooperative node (graph_norm) instead of two
+    bool graph_onepass = false;  // one node, the one-launch step (graph_norm), not two
 
     // Checkpoint writing: options and the writer thread.
     int32_t keep = 0;                   // rotation: newest files kept (0 = all)
