@@ -61,12 +61,12 @@ int cuda_fail(cudaError_t e, const char* what)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Whether the graph takes the one-launch step (the same rule as
-// adamw_clip_step's).
-// The one-launch node only in its cluster form (up to 65,536 parameters):
-// in a graph, with no launch overhead to save, the two-node step costs less
-// GPU time than the cooperative grid above that size.  The barrier-timeout
-// test flag asks for the grid (its next graph step rebuilds the graph).
+// Whether the graph takes the one-launch step -- the rule adamw_clip_step
+// follows when its stream is being captured: the one-launch node only in its
+// cluster form (up to 65,536 parameters), since in a graph, with no launch
+// overhead to save, the two-node step costs less GPU time than the
+// cooperative grid above that size.  The barrier-timeout test flag asks for
+// the grid (its next graph step rebuilds the graph).
 bool want_onepass(const adamw_ctx* c)
 {
     return c->onepass && c->n <= c->onepass_max_n &&
