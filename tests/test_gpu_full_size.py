@@ -3,7 +3,8 @@
 The 110M tensor list (196 tensors, n = 110,418,432; the fused kernel hands
 its chunks out by a counter at this size) and the flat 2^30-parameter (1B)
 state, one step at t = 7 from generator-made non-zero moments, so that both
-bias corrections and both moment terms are in play.  On the 110M list:
+bias corrections and both moment terms are in play; and the flat 12.8M
+configuration's whole 100-step trajectory.  On the 110M list:
 
 * float32 gradient, decay on every parameter;
 * decay flags exempting every 1-D tensor (biases, LayerNorm gains and
@@ -26,7 +27,7 @@ import pytest
 import synthetic
 from synthetic import device as synth_dev
 from synthetic import workloads as W
-from parity import FLOOR, RTOL_NORM, RTOL_ONE_STEP, magnitudes
+from parity import FLOOR, RTOL_NORM, RTOL_ONE_STEP, RTOL_TRAJECTORY, Running, magnitudes
 
 torch = pytest.importorskip("torch")
 import optimizer_step_resumable_gb300 as osr  # noqa: E402
@@ -159,3 +160,53 @@ def test_flat_1b_one_step_every_element(dev, oracle):
     del w, g, m, v
     torch.cuda.empty_cache()
     _check_all(oracle, got, hw, hg, hm, hv, s, wl.lr, _chunks([0], [n], wl.wd), "flat 2^30")
+
+
+def test_flat_12m8_100_step_trajectory_every_element(dev, oracle):
+    """The 12.8M configuration (flat, g ~ 1e-3, every step clipped): 100
+    steps on the GPU and, beside them, the oracle's own 100-step trajectory
+    of every element from the same generator inputs (its clip factor from its
+    own norm each step), run in index chunks on all host cores.  Each step's
+    norm within 1e-6 of the oracle's; after 100 steps every element of w, m
+    and v within the trajectory bar (1e-5 of the magnitudes carried along the
+    oracle's trajectory, tests/parity.py)."""
+    wl = W.flat_12m8()
+    n = wl.n
+    w = torch.empty(n, device=dev)
+    g = torch.empty(n, device=dev)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    synth_dev.fill_weights(w, wl.seed)
+    ow = w.cpu().numpy()
+    om = np.zeros(n, np.float32)
+    ov = np.zeros(n, np.float32)
+    chunk = 1 << 20
+    spans = [(lo, min(lo + chunk, n)) for lo in range(0, n, chunk)]
+    runs = [Running() for _ in spans]
+    mags = [None] * len(spans)
+
+    def advance(i, hg, s, t):
+        lo, hi = spans[i]
+        idx = np.arange(lo, hi, dtype=np.int64)
+        terms = oracle.adamw_terms_at(idx, ow, hg, om, ov, s, t, wl.lr, wl.wd)
+        mags[i] = runs[i].update(terms, wl.lr, wl.wd, t)
+        nw, nm, nv = oracle.adamw_at(idx, ow, hg, om, ov, s, t, wl.lr, wl.wd)
+        ow[lo:hi], om[lo:hi], ov[lo:hi] = nw, nm, nv
+
+    with osr.adamw_create(n, flags=osr.CREATE_NO_CKPT) as ctx, \
+            ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        for t in range(1, wl.steps + 1):
+            synth_dev.fill_grads(g, wl.seed, t, wl.grad_sigma)
+            hg = g.cpu().numpy()
+            osr.adamw_clip_step(ctx, w, g, m, v, t, wl.lr, wl.wd, wl.clip)
+            onorm = oracle.global_norm(hg)
+            s = oracle.clip_scale(onorm, wl.clip)
+            list(ex.map(lambda i: advance(i, hg, s, t), range(len(spans))))
+            norm, _ = osr.adamw_last_norm(ctx)
+            assert abs(norm - onorm) <= RTOL_NORM * onorm, (t, norm, onorm)
+    got = [x.cpu().numpy() for x in (w, m, v)]
+    full = [np.concatenate([mg[k] for mg in mags]) for k in range(3)]
+    for name, a, o, mag in zip("wmv", got, (ow, om, ov), full):
+        err = np.abs(a.astype(np.float64) - o.astype(np.float64))
+        bad = np.nonzero(~(err <= RTOL_TRAJECTORY * mag + FLOOR))[0]
+        assert bad.size == 0, (name, bad.size, int(bad[0]), a[bad[0]], o[bad[0]], mag[bad[0]])
