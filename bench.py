@@ -446,6 +446,19 @@ def oracle_rates(wl, seconds):
     return out
 
 
+def _guarded(fn, *args):
+    """fn(*args), or {"error": ...} if it raises (for example when a state of
+    2^30 parameters, or its pinned checkpoint image, does not fit), so that
+    one configuration cannot cost the bench line."""
+    import torch
+    try:
+        return fn(*args)
+    except Exception as e:  # noqa: BLE001 -- reported in the line instead
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        return {"error": f"{type(e).__name__}: {e}"[:300]}
+
+
 def config_throughput(name, K, W, dev, main, side, peak, cpu_seconds):
     """params/s of the library's default step on one flat workload (inputs
     resident; above L2 for 12.8M and up), each kernel's rate from a second
@@ -760,9 +773,10 @@ def run_ours(args):
     if world == 1 and not args.no_configs:
         cs = max(1.0, args.cpu_seconds / 4)
         line["per_config"] = {
-            "flat-2^30": config_throughput("flat-2^30", K, W, dev, main, side, peak, cs),
-            "flat-12.8M": config_throughput("flat-12.8M", K, W, dev, main, side, peak, cs),
-            "flat-65536": config_latency(dev, main, cs),
+            "flat-2^30": _guarded(config_throughput, "flat-2^30", K, W, dev, main, side, peak, cs),
+            "flat-12.8M": _guarded(config_throughput, "flat-12.8M", K, W, dev, main, side, peak,
+                                   cs),
+            "flat-65536": _guarded(config_latency, dev, main, cs),
         }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
