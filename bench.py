@@ -454,8 +454,11 @@ def _guarded(fn, *args):
     try:
         return fn(*args)
     except Exception as e:  # noqa: BLE001 -- reported in the line instead
-        torch.cuda.synchronize()
-        torch.cuda.empty_cache()
+        try:
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        except Exception:  # noqa: BLE001 -- the error above is the one reported
+            pass
         return {"error": f"{type(e).__name__}: {e}"[:300]}
 
 
