@@ -87,3 +87,11 @@ def test_kernel_stats_rates_and_fractions():
     assert ks["k_clip_adamw"]["GB/s"] == pytest.approx(28 * n / 0.01 / 1e6)  # 2800 GB/s
     assert ks["k_clip_adamw"]["frac"] == pytest.approx(1.4)
     assert ks["k_clip_adamw"]["frac_of_nominal_8tbs"] == pytest.approx(2800 / 8000)
+
+
+def test_guarded_config_reports_its_error():
+    def boom(x):
+        raise MemoryError(f"no room for {x}")
+    out = bench._guarded(boom, "flat-2^30")
+    assert out == {"error": "MemoryError: no room for flat-2^30"}
+    assert bench._guarded(lambda a, b: a + b, 2, 3) == 5
